@@ -1,0 +1,401 @@
+#!/usr/bin/env python3
+"""Throughput of the device-wide single-pass scan on GB300.
+
+One step is one call of the C entry point dwp_scan_exclusive (u32 addition)
+over n = 2^28 full-range values already resident in HBM: scratch clear plus
+the single-pass scan kernel, i.e. every step of the plain scan's hot path.
+The input (1 GiB) and output (1 GiB) are each larger than the 129 MB L2, so
+no L2 flush is needed between steps.
+
+Printed (rank 0, one JSON line): Gelem/s of the whole job, the roofline of the
+scan kernel against the measured HBM copy bandwidth, the same metric end to
+end from pinned host memory (copies inside the timed region), the oracle
+timed on the host cores, SM clocks sampled during the timed region, and the
+other scans, the segmented scan and the compaction measured the same way
+under "secondary".
+
+--impl reference times the sequential CPU oracle instead (the only other
+place this script runs oracle code), on a bounded slice of the same input.
+With torchrun (N > 1) every rank scans its own replica of the input (no
+collective on the data path); rank 0 reports max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "u32 exclusive scan Gelem/s and HBM GB/s as % of peak at n=2^28; segscan Gelem/s"
+N_FULL = 1 << 28
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "scan_u32_exclusive_2p28.md")
+KERNEL_SOURCES = ["device_wide_prefix_gb300/csrc/scan.cu", "device_wide_prefix_gb300/csrc/device.cuh"]
+
+
+def kernel_hash(paths=KERNEL_SOURCES) -> str:
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def profiled_traffic(summary=PROFILE_SUMMARY, sources=KERNEL_SOURCES):
+    """dram bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    if not os.path.exists(summary):
+        return None
+    fields = {}
+    with open(summary) as f:
+        for line in f:
+            if ":" in line and line.strip().startswith("- "):
+                k, v = line.strip()[2:].split(":", 1)
+                fields[k.strip()] = v.strip().strip("`")
+    if fields.get("kernel_source_sha256_16") != kernel_hash(sources):
+        return None
+    try:
+        return int(fields["dram_bytes_per_launch_full_size"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (100 ms) while running; summary of those inside a window."""
+
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    @staticmethod
+    def _ts(s: str) -> float:
+        s = s.strip()
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return time.mktime(time.strptime(s.split(".")[0], fmt.split(".")[0])) + (
+                    float("0." + s.split(".")[1]) if "." in s else 0.0)
+            except ValueError:
+                continue
+        return 0.0
+
+    def summary(self, t0: float, t1: float) -> dict:
+        rows = []
+        for row in csv.reader(io.StringIO("\n".join(self.lines))):
+            if len(row) < 10:
+                continue
+            try:
+                rows.append({"t": self._ts(row[0]), "sm": float(row[2]), "max": float(row[3]),
+                             "power": float(row[4]) if row[4].strip() not in ("[N/A]", "") else 0.0,
+                             "hw_slowdown": row[6].strip(), "hw_thermal": row[7].strip(),
+                             "sw_thermal": row[8].strip(), "sw_power_cap": row[9].strip()})
+            except ValueError:
+                continue
+        inside = [r for r in rows if t0 - 0.05 <= r["t"] <= t1 + 0.05]
+        used = inside if inside else rows[-3:]
+        if not used:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "no nvidia-smi samples"}
+        reasons = set()
+        for r in used:
+            for key, name in (("hw_slowdown", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                              ("sw_thermal", "sw_thermal_slowdown"),
+                              ("sw_power_cap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median([r["sm"] for r in used])),
+                "sm_max_mhz": max(r["max"] for r in used), "reasons": sorted(reasons),
+                "samples": len(used), "power_w_max": max(r["power"] for r in used),
+                "window": "timed region" if inside else "last samples (timed region shorter than the sampling period)"}
+
+
+# ---------------------------------------------------------------- reference arm
+
+def run_reference(args, rank: int) -> None:
+    if rank != 0:
+        return
+    import oracle
+    ref = oracle.Oracle()
+    x = synth.u32_full_values(N_FULL)
+    # calibrate, then size each step so the whole run stays near 60 s
+    t = time.perf_counter()
+    ref.scan_u32_add(x[: 1 << 22], False)
+    rate = (1 << 22) / max(time.perf_counter() - t, 1e-6)
+    per_step = int(min(N_FULL, max(1 << 20, 60.0 * rate / max(args.steps + args.warmup, 1))))
+    per_step -= per_step % 4
+    sl = x[:per_step]
+    for _ in range(args.warmup):
+        ref.scan_u32_add(sl, False)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        ref.scan_u32_add(sl, False)
+    dt = time.perf_counter() - t0
+    val = per_step * args.steps / dt / 1e9
+    sample = "first %d elements of the n=2^28 full-range u32 input per step" % per_step
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "Gelem/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32",
+        "data": "synthetic (SplitMix64 seed 0xD3B00002)",
+        "config": {"workload": "u32 exclusive sum scan, n=2^28, values uniform in [0, 2^32)",
+                   "n": N_FULL, "sample_elements_per_step": per_step},
+        "cpu_baseline": {"value": val, "unit": "Gelem/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": val, "unit": "Gelem/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- our arm
+
+def main() -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=10.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    args.steps = max(args.steps, 1)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+
+    import torch
+    import device_wide_prefix_gb300 as dwp
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    lib = dwp.load()
+    stream = torch.cuda.current_stream(dev)
+    sptr = int(stream.cuda_stream)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    def max_over_ranks(v: float) -> float:
+        if dist is None:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    import ctypes
+    n = N_FULL
+    x_host = torch.from_numpy(synth.u32_full_values(n).view(np.int32)).pin_memory()
+    x = x_host.to(dev)
+    y = torch.empty_like(x)
+    need = dwp.scan_scratch_bytes(n)
+    scratch = dwp.alloc_scratch(need, dev)
+    sb = ctypes.c_size_t(need)
+    f = lib.dwp_scan_exclusive
+    a_in, a_out, a_s = ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(y.data_ptr()), ctypes.c_void_p(scratch.data_ptr())
+    a_st = ctypes.c_void_p(sptr)
+
+    def step():
+        st = f(dwp.DWP_U32_ADD, a_in, a_out, n, a_s, ctypes.byref(sb), a_st)
+        if st != 0:
+            raise RuntimeError(dwp.status_string(st))
+
+    clocks = ClockSampler(local_rank) if rank == 0 else None
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    if dwp.read_status(scratch) != dwp.DWP_SUCCESS:
+        raise RuntimeError("device status after warm-up: %s" % dwp.status_string(dwp.read_status(scratch)))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    wall0 = time.time()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    barrier()
+    wall1 = time.time()
+    st = dwp.read_status(scratch)
+    if st != dwp.DWP_SUCCESS:
+        raise RuntimeError("device status after timed steps: %s" % dwp.status_string(st))
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps)
+    value = world * n / (ms * 1e-3) / 1e9
+
+    # end to end from pinned host memory through the same C entry point
+    e2e_steps = max(3, min(args.steps, 20))
+    y_host = torch.empty(n, dtype=torch.int32).pin_memory()
+    for _ in range(2):
+        x.copy_(x_host, non_blocking=True); step(); y_host.copy_(y, non_blocking=True)
+    barrier()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        x.copy_(x_host, non_blocking=True)
+        step()
+        y_host.copy_(y, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps)
+    if clocks is not None:
+        clocks.stop()
+
+    peaks = measured_peaks()
+    alg_bytes = 8 * n
+    achieved = alg_bytes / (ms * 1e-3) / 1e9
+
+    secondary = {}
+    if not args.no_secondary and rank == 0:
+        secondary = measure_secondary(dwp, lib, dev, stream, peaks, x, y, scratch, need)
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    cpu = cpu_baseline(x_host.numpy().view(np.uint32), args.cpu_budget_s)
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "Gelem/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "u32",
+        "data": "synthetic (SplitMix64 seed 0xD3B00002, values uniform in [0, 2^32))",
+        "config": {"workload": "u32 exclusive sum scan, n=2^28, values uniform in [0, 2^32)",
+                   "n": n, "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (1 GiB in + 1 GiB out vs 129 MB L2); no flush"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)",
+                     "algorithmic_bytes_per_launch": alg_bytes,
+                     "timing": "CUDA events over the whole C call (scratch clear + scan kernel)",
+                     "traffic": profiled_traffic()},
+        "cpu_baseline": cpu,
+        "e2e": {"value": n / (e2e_ms * 1e-3) / 1e9, "unit": "Gelem/s",
+                "h2d_bytes_per_step": 4 * n, "d2h_bytes_per_step": 4 * n,
+                "ms_per_step": e2e_ms, "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": clocks.summary(wall0, wall1) if clocks is not None else None,
+        "secondary": secondary,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def cpu_baseline(x: np.ndarray, budget_s: float) -> dict:
+    import oracle
+    ref = oracle.Oracle()
+    runs, t_total = 0, 0.0
+    while t_total < budget_s or runs == 0:
+        t = time.perf_counter()
+        ref.scan_u32_add(x, False)
+        t_total += time.perf_counter() - t
+        runs += 1
+        if runs >= 100:
+            break
+    return {"value": runs * x.size / t_total / 1e9, "unit": "Gelem/s", "cores": 1, "kind": "oracle",
+            "sample": "%d full passes over the n=2^28 input (%.1f s), sequential C oracle on one host core"
+                      % (runs, t_total)}
+
+
+def time_calls(fn, steps: int, warmup: int, stream) -> float:
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def measure_secondary(dwp, lib, dev, stream, peaks, x, y, scratch, need) -> dict:
+    import ctypes
+    n = x.numel()
+    out = {}
+    sb = ctypes.c_size_t(need)
+    st_ptr = ctypes.c_void_p(int(stream.cuda_stream))
+    xf = None
+    for name, entry, op in (("u32_add_inclusive", lib.dwp_scan_inclusive, dwp.DWP_U32_ADD),
+                            ("u32_max_exclusive", lib.dwp_scan_exclusive, dwp.DWP_U32_MAX),
+                            ("u32_max_inclusive", lib.dwp_scan_inclusive, dwp.DWP_U32_MAX),
+                            ("f32_add_inclusive", lib.dwp_scan_inclusive, dwp.DWP_F32_ADD)):
+        src = x
+        if op == dwp.DWP_F32_ADD:
+            import torch
+            xf = torch.from_numpy(synth.f32_values(n)).to(dev)
+            src = xf
+        args = (op, ctypes.c_void_p(src.data_ptr()), ctypes.c_void_p(y.data_ptr()), n,
+                ctypes.c_void_p(scratch.data_ptr()), ctypes.byref(sb), st_ptr)
+        ms = time_calls(lambda: entry(*args), 200, 5, stream)
+        gbs = 8 * n / (ms * 1e-3) / 1e9
+        out[name] = {"n": n, "ms": ms, "Gelem_s": n / (ms * 1e-3) / 1e9, "GB_s": gbs,
+                     "frac": gbs / peaks["hbm_gbs"]}
+    return out
+
+
+if __name__ == "__main__":
+    main()

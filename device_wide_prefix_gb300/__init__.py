@@ -1,0 +1,203 @@
+"""device_wide_prefix_gb300: Python binding of libdwp.so (include/dwp.h).
+
+The binding only marshals arguments: every step of every operation runs in
+the library's CUDA kernels.  PyTorch supplies device memory and streams.
+There is no CPU fallback: if libdwp.so is missing or cannot be loaded, every
+call raises.
+
+Two layers:
+  * the C entry points under their C names (dwp_scan_exclusive, ...), taking
+    integer device addresses and returning the integer dwp_status;
+  * tensor helpers (scan_exclusive, scan_inclusive, ...) that size and
+    allocate the scratch with torch, call the C entry point on the current
+    stream of the tensors' device and raise DwpError on a non-zero status.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libdwp.so")
+
+DWP_SUCCESS = 0
+DWP_ERR_INVALID_VALUE = 1
+DWP_ERR_MISALIGNED = 2
+DWP_ERR_ALIASING = 3
+DWP_ERR_SCRATCH_TOO_SMALL = 4
+DWP_ERR_CUDA = 5
+DWP_ERR_LOOKBACK_TIMEOUT = 6
+DWP_ERR_PIPELINE_TIMEOUT = 7
+DWP_ERR_NO_DEVICE = 8
+
+DWP_U32_ADD = 0
+DWP_F32_ADD = 1
+DWP_U32_MAX = 2
+OPS = {"u32_add": DWP_U32_ADD, "f32_add": DWP_F32_ADD, "u32_max": DWP_U32_MAX}
+
+DWP_EXCLUSIVE = 0
+DWP_INCLUSIVE = 1
+
+# Names the C header declares (checked by the tests against include/dwp.h).
+EXPORTS = [
+    "dwp_scan_exclusive",
+    "dwp_scan_inclusive",
+    "dwp_read_status",
+    "dwp_status_string",
+    "dwp_version",
+    "dwp_debug_set_fault",
+]
+
+_lib = None
+
+
+class DwpError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__("%s failed: %s" % (what, status_string(status)))
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libdwp.so and declare its entry points.  Raises if it is missing."""
+    global _lib
+    if _lib is not None and path == LIB_PATH:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(
+            "libdwp.so is not built (%s); run `python -c \"import __graft_entry__ as g; g.build()\"`"
+            % path)
+    lib = ctypes.CDLL(path)
+    c = ctypes
+    P, S, Z = c.c_void_p, c.c_size_t, c.POINTER(c.c_size_t)
+    for name in ("dwp_scan_exclusive", "dwp_scan_inclusive"):
+        f = getattr(lib, name)
+        f.argtypes = [c.c_int, P, P, S, P, Z, P]
+        f.restype = c.c_int
+    lib.dwp_read_status.argtypes = [P, P]
+    lib.dwp_read_status.restype = c.c_int
+    lib.dwp_status_string.argtypes = [c.c_int]
+    lib.dwp_status_string.restype = c.c_char_p
+    lib.dwp_version.argtypes = []
+    lib.dwp_version.restype = c.c_int
+    lib.dwp_debug_set_fault.argtypes = [c.c_uint32, c.c_uint32]
+    lib.dwp_debug_set_fault.restype = c.c_int
+    if path == LIB_PATH:
+        _lib = lib
+    return lib
+
+
+# ---------------------------------------------------------------------------
+# C entry points under their C names (integer addresses in, status out)
+
+
+def _scan_entry(name, op, d_in, d_out, n, d_scratch, scratch_bytes, stream):
+    sb = ctypes.c_size_t(scratch_bytes)
+    st = getattr(load(), name)(int(op), d_in or None, d_out or None, n, d_scratch or None,
+                               ctypes.byref(sb), stream or None)
+    return st, sb.value
+
+
+def dwp_scan_exclusive(op, d_in, d_out, n, d_scratch, scratch_bytes, stream):
+    """dwp.h dwp_scan_exclusive; returns (status, scratch_bytes after the call)."""
+    return _scan_entry("dwp_scan_exclusive", op, d_in, d_out, n, d_scratch, scratch_bytes, stream)
+
+
+def dwp_scan_inclusive(op, d_in, d_out, n, d_scratch, scratch_bytes, stream):
+    """dwp.h dwp_scan_inclusive; returns (status, scratch_bytes after the call)."""
+    return _scan_entry("dwp_scan_inclusive", op, d_in, d_out, n, d_scratch, scratch_bytes, stream)
+
+
+def dwp_read_status(d_scratch, stream) -> int:
+    return load().dwp_read_status(d_scratch or None, stream or None)
+
+
+def dwp_status_string(status: int) -> str:
+    return load().dwp_status_string(int(status)).decode()
+
+
+def dwp_version() -> int:
+    return load().dwp_version()
+
+
+def dwp_debug_set_fault(never_publish_tile: int, spin_limit: int) -> int:
+    return load().dwp_debug_set_fault(never_publish_tile & 0xFFFFFFFF, spin_limit)
+
+
+def status_string(status: int) -> str:
+    try:
+        return dwp_status_string(status)
+    except Exception:  # library not loadable: still give a readable message
+        return "status %d" % status
+
+
+def _check(st: int, what: str) -> None:
+    if st != DWP_SUCCESS:
+        raise DwpError(st, what)
+
+
+# ---------------------------------------------------------------------------
+# tensor helpers (torch is the memory and stream provider only)
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_of(t, stream=None) -> int:
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream(t.device)
+    return int(stream.cuda_stream)
+
+
+def _scan_dtype(op: str):
+    torch = _torch()
+    return torch.float32 if op == "f32_add" else torch.int32
+
+
+def scan_scratch_bytes(n: int, op: str = "u32_add") -> int:
+    st, b = dwp_scan_exclusive(OPS[op], None, None, n, None, 0, None)
+    _check(st, "scratch size query")
+    return b
+
+
+def alloc_scratch(nbytes: int, device):
+    """A scratch buffer from torch's caching allocator (16-byte aligned)."""
+    torch = _torch()
+    return torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=device)
+
+
+def _scan(inclusive: bool, x, op: str, out=None, scratch=None, stream=None):
+    torch = _torch()
+    if op not in OPS:
+        raise ValueError("unknown op %r" % op)
+    if not x.is_cuda or not x.is_contiguous() or x.element_size() != 4:
+        raise ValueError("x must be a contiguous CUDA tensor of 4-byte elements")
+    n = x.numel()
+    if out is None:
+        out = torch.empty_like(x)
+    need = scan_scratch_bytes(n, op)
+    if scratch is None:
+        scratch = alloc_scratch(need, x.device)
+    entry = dwp_scan_inclusive if inclusive else dwp_scan_exclusive
+    with torch.cuda.device(x.device):
+        st, _ = entry(OPS[op], x.data_ptr(), out.data_ptr(), n, scratch.data_ptr(),
+                      scratch.numel(), _stream_of(x, stream))
+    _check(st, "dwp_scan_inclusive" if inclusive else "dwp_scan_exclusive")
+    return out
+
+
+def scan_exclusive(x, op: str = "u32_add", out=None, scratch=None, stream=None):
+    """Exclusive scan of a contiguous CUDA tensor (int32/uint32 bits or float32)."""
+    return _scan(False, x, op, out, scratch, stream)
+
+
+def scan_inclusive(x, op: str = "u32_add", out=None, scratch=None, stream=None):
+    """Inclusive scan of a contiguous CUDA tensor (int32/uint32 bits or float32)."""
+    return _scan(True, x, op, out, scratch, stream)
+
+
+def read_status(scratch, stream=None) -> int:
+    """Device-side status of the last call that used `scratch` (synchronises)."""
+    return dwp_read_status(scratch.data_ptr(), _stream_of(scratch, stream))

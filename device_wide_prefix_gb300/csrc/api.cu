@@ -1,0 +1,110 @@
+// C entry points: argument validation, the scratch size query, the scratch
+// clear and the launch.  Validation happens before any CUDA call, so an
+// argument error never enqueues work.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "launch.h"
+
+namespace {
+
+using namespace dwp;
+
+constexpr uint64_t kMaxN = 0xffffffffull;  // n < 2^32
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Do [a, a+an) and [b, b+bn) share a byte?
+bool overlap(const void *a, uint64_t an, const void *b, uint64_t bn) {
+    if (!a || !b || an == 0 || bn == 0) return false;
+    const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+    return pa < pb + bn && pb < pa + an;
+}
+
+uint64_t ceil_div(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
+
+dwp_status scan_common(bool inclusive, dwp_op op, const void *in, void *out, size_t n,
+                       void *scratch, size_t *scratch_bytes, dwp_stream stream) {
+    if (!scratch_bytes) return DWP_ERR_INVALID_VALUE;
+    const int iop = static_cast<int>(op);
+    if (iop != DWP_U32_ADD && iop != DWP_F32_ADD && iop != DWP_U32_MAX) return DWP_ERR_INVALID_VALUE;
+    if (uint64_t(n) > kMaxN) return DWP_ERR_INVALID_VALUE;
+    const uint64_t tiles = ceil_div(n, scan_tile_elems());
+    const size_t need = scratch_bytes_for_tiles(tiles);
+    if (!scratch) {
+        *scratch_bytes = need;
+        return DWP_SUCCESS;
+    }
+    if (*scratch_bytes < need) return DWP_ERR_SCRATCH_TOO_SMALL;
+    if (n > 0 && (!in || !out)) return DWP_ERR_INVALID_VALUE;
+    if (!aligned16(scratch) || (n > 0 && (!aligned16(in) || !aligned16(out))))
+        return DWP_ERR_MISALIGNED;
+    const uint64_t bytes = uint64_t(n) * 4u;
+    if (in != out && overlap(in, bytes, out, bytes)) return DWP_ERR_ALIASING;
+    if (overlap(scratch, need, in, bytes) || overlap(scratch, need, out, bytes))
+        return DWP_ERR_ALIASING;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(scratch, 0, need, s) != cudaSuccess) {
+        cudaGetLastError();
+        return DWP_ERR_CUDA;
+    }
+    if (n == 0) return DWP_SUCCESS;
+    if (launch_scan(op, inclusive, in, out, n, scratch, s) != cudaSuccess) {
+        cudaGetLastError();
+        return DWP_ERR_CUDA;
+    }
+    return DWP_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" {
+
+dwp_status dwp_scan_exclusive(dwp_op op, const void *d_in, void *d_out, size_t n,
+                              void *d_scratch, size_t *scratch_bytes, dwp_stream stream) {
+    return scan_common(false, op, d_in, d_out, n, d_scratch, scratch_bytes, stream);
+}
+
+dwp_status dwp_scan_inclusive(dwp_op op, const void *d_in, void *d_out, size_t n,
+                              void *d_scratch, size_t *scratch_bytes, dwp_stream stream) {
+    return scan_common(true, op, d_in, d_out, n, d_scratch, scratch_bytes, stream);
+}
+
+dwp_status dwp_read_status(const void *d_scratch, dwp_stream stream) {
+    if (!d_scratch) return DWP_ERR_INVALID_VALUE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t st = 0;
+    const auto *hdr = reinterpret_cast<const ScratchHeader *>(d_scratch);
+    if (cudaMemcpyAsync(&st, &hdr->status, sizeof(st), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return DWP_ERR_CUDA;
+    }
+    return static_cast<dwp_status>(st);
+}
+
+const char *dwp_status_string(dwp_status status) {
+    switch (status) {
+        case DWP_SUCCESS: return "DWP_SUCCESS";
+        case DWP_ERR_INVALID_VALUE: return "DWP_ERR_INVALID_VALUE";
+        case DWP_ERR_MISALIGNED: return "DWP_ERR_MISALIGNED";
+        case DWP_ERR_ALIASING: return "DWP_ERR_ALIASING";
+        case DWP_ERR_SCRATCH_TOO_SMALL: return "DWP_ERR_SCRATCH_TOO_SMALL";
+        case DWP_ERR_CUDA: return "DWP_ERR_CUDA";
+        case DWP_ERR_LOOKBACK_TIMEOUT: return "DWP_ERR_LOOKBACK_TIMEOUT";
+        case DWP_ERR_PIPELINE_TIMEOUT: return "DWP_ERR_PIPELINE_TIMEOUT";
+        case DWP_ERR_NO_DEVICE: return "DWP_ERR_NO_DEVICE";
+    }
+    return "DWP_UNKNOWN_STATUS";
+}
+
+int dwp_version(void) { return 100; }
+
+dwp_status dwp_debug_set_fault(uint32_t never_publish_tile, uint32_t spin_limit) {
+    set_fault_config(never_publish_tile, spin_limit);
+    return DWP_SUCCESS;
+}
+
+}  // extern "C"

@@ -1,0 +1,22 @@
+// Host-side launch helpers and the kernel launchers behind the C entry points.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "common.h"
+
+namespace dwp {
+
+// Resident blocks of `kernel` on the current device (SM count x blocks per
+// SM at this block size and dynamic shared memory).  Also raises the
+// kernel's dynamic shared-memory limit to `smem_bytes`.  Cached per device
+// and kernel.  Returns 0 if the kernel cannot be resident at all.
+int device_blocks(const void *kernel, int threads, size_t smem_bytes);
+
+// Elements per tile of the plain scan kernel.
+uint32_t scan_tile_elems();
+// One launch of the plain scan (the scratch has already been cleared).
+cudaError_t launch_scan(dwp_op op, bool inclusive, const void *in, void *out, uint64_t n,
+                        void *scratch, cudaStream_t stream);
+
+}  // namespace dwp

@@ -1,0 +1,135 @@
+/*
+ * dwp.h - device-wide single-pass prefix scan for NVIDIA GB300 (sm_103a).
+ *
+ * C ABI.  Every entry point takes plain device pointers and sizes, runs as
+ * one stream-ordered launch sequence on the caller's stream and returns
+ * without synchronising.  The library never allocates memory: the caller
+ * owns inputs, outputs and scratch.
+ *
+ * Operation ("Parallel Prefix Sum (Scan), in depth", section "Inclusive,
+ * exclusive and associative"): for an associative operator (+) with identity
+ * e, the inclusive scan is y[i] = x[0] (+) ... (+) x[i]; the exclusive scan
+ * is y[0] = e and y[i] = x[0] (+) ... (+) x[i-1].  Identities ("Prefix scans
+ * and compaction", section "Inclusive and exclusive scan"): 0 for addition,
+ * the lowest representable value (0 for u32) for a maximum.
+ *
+ * Method ("Single-Pass Prefix Scan with Decoupled Look-Back", sections
+ * "Three states in a per-block descriptor" and "The publication protocol in
+ * code"; "Parallel Prefix Sum (Scan), in depth", section "Scanning a whole
+ * array: three grid strategies"): one pass over the data.  Tiles take their
+ * index from an atomic counter, publish their aggregate in a 64-bit
+ * descriptor (state and value in one word), look back over their
+ * predecessors' descriptors until an inclusive prefix is found, publish
+ * their own inclusive prefix and write their output.
+ *
+ * Scratch (two-call pattern, "Parallel Prefix Sum (Scan), in depth",
+ * section "Use the library"): call once with d_scratch == NULL to receive
+ * the required byte count in *scratch_bytes, then again with a device
+ * buffer of at least that many bytes.  The scratch holds the tile counter,
+ * a device-side status word and one 8-byte descriptor per tile; each call
+ * clears the part it uses with a cudaMemsetAsync on `stream` before its
+ * kernel.  Calls that share one scratch buffer must be ordered (same stream
+ * or synchronised); overlapping calls on one scratch buffer race.
+ *
+ * Pointers: every data pointer and the scratch pointer must be 16-byte
+ * aligned (DWP_ERR_MISALIGNED otherwise).  Sizes: n < 2^32.
+ *
+ * Errors: argument errors are reported before anything is enqueued.  A
+ * launch error is DWP_ERR_CUDA.  Errors that arise on the device (a
+ * look-back or pipeline wait that ran past its limit) are recorded in the
+ * scratch status word and returned by dwp_read_status().  All device-side
+ * waits are bounded: a kernel never hangs, it records an error and exits.
+ */
+#ifndef DWP_H
+#define DWP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream handle; the same value as a cudaStream_t.  NULL means the
+ * legacy default stream. */
+typedef struct CUstream_st *dwp_stream;
+
+typedef enum dwp_status {
+    DWP_SUCCESS = 0,
+    DWP_ERR_INVALID_VALUE = 1,     /* null pointer with n > 0, unknown op/mode, n >= 2^32 */
+    DWP_ERR_MISALIGNED = 2,        /* a pointer is not 16-byte aligned */
+    DWP_ERR_ALIASING = 3,          /* input, output or scratch ranges overlap (see each call) */
+    DWP_ERR_SCRATCH_TOO_SMALL = 4, /* *scratch_bytes is below the size query's answer */
+    DWP_ERR_CUDA = 5,              /* a CUDA runtime call or launch failed */
+    DWP_ERR_LOOKBACK_TIMEOUT = 6,  /* device: a look-back spin ran past its limit */
+    DWP_ERR_PIPELINE_TIMEOUT = 7,  /* device: a shared-memory pipeline wait ran past its limit */
+    DWP_ERR_NO_DEVICE = 8          /* no usable CUDA device */
+} dwp_status;
+
+/* Associative operators of the plain scans. */
+typedef enum dwp_op {
+    DWP_U32_ADD = 0, /* uint32 addition, wraps modulo 2^32; identity 0 */
+    DWP_F32_ADD = 1, /* float32 addition in f32 arithmetic; identity +0.0f */
+    DWP_U32_MAX = 2  /* uint32 maximum; identity 0 */
+} dwp_op;
+
+typedef enum dwp_mode {
+    DWP_EXCLUSIVE = 0,
+    DWP_INCLUSIVE = 1
+} dwp_mode;
+
+/*
+ * Exclusive scan of n elements of d_in (uint32 or float32 per `op`) into
+ * d_out.  Definition: "Parallel Prefix Sum (Scan), in depth", section
+ * "Inclusive, exclusive and associative"; y[0] is the identity.
+ *   op            DWP_U32_ADD, DWP_F32_ADD or DWP_U32_MAX
+ *   d_in, d_out   device arrays of n 4-byte elements, contiguous.
+ *                 d_out == d_in (exact in-place) is allowed; any other
+ *                 overlap is DWP_ERR_ALIASING.
+ *   n             element count, 0 <= n < 2^32; n == 0 enqueues only the
+ *                 scratch clear.
+ *   d_scratch     NULL for the size query, else a device buffer that does
+ *                 not overlap d_in or d_out.
+ *   scratch_bytes in: size of d_scratch; out (size query): size needed.
+ *   stream        stream the work is enqueued on.
+ * f32 results are not bit-reproducible from run to run: the grouping of the
+ * partial sums depends on look-back timing ("Single-Pass Prefix Scan with
+ * Decoupled Look-Back", section "When not to use it").
+ */
+dwp_status dwp_scan_exclusive(dwp_op op, const void *d_in, void *d_out, size_t n,
+                              void *d_scratch, size_t *scratch_bytes, dwp_stream stream);
+
+/* Inclusive scan; arguments as dwp_scan_exclusive.  y[i] includes x[i]. */
+dwp_status dwp_scan_inclusive(dwp_op op, const void *d_in, void *d_out, size_t n,
+                              void *d_scratch, size_t *scratch_bytes, dwp_stream stream);
+
+/*
+ * Device-side status of the most recent call that used d_scratch.
+ * Synchronises `stream`, then reads the status word.  Returns DWP_SUCCESS,
+ * DWP_ERR_LOOKBACK_TIMEOUT or DWP_ERR_PIPELINE_TIMEOUT; DWP_ERR_CUDA if the
+ * synchronisation or the read fails; DWP_ERR_INVALID_VALUE for NULL.
+ */
+dwp_status dwp_read_status(const void *d_scratch, dwp_stream stream);
+
+/* Static, NUL-terminated name of a status code. */
+const char *dwp_status_string(dwp_status status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int dwp_version(void);
+
+/*
+ * Test hook, not for production use.  For every later call in this process
+ * until reset: the tile with index `never_publish_tile` does its work but
+ * never publishes its descriptor (UINT32_MAX disables this), and look-back
+ * spins give up after `spin_limit` polls (0 restores the default, about a
+ * second of polling).  The successors of the silent tile then record
+ * DWP_ERR_LOOKBACK_TIMEOUT in the scratch status and exit instead of
+ * waiting forever.  Not thread-safe; affects every device.
+ */
+dwp_status dwp_debug_set_fault(uint32_t never_publish_tile, uint32_t spin_limit);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DWP_H */

@@ -1,0 +1,97 @@
+"""The C-ABI library without a GPU: it loads, exports every symbol the header
+declares, and its host-side validation rejects bad arguments before any CUDA
+call (fake, never-dereferenced addresses are enough for that)."""
+import os
+import re
+
+import pytest
+
+import device_wide_prefix_gb300 as dwp
+from device_wide_prefix_gb300 import build as dwp_build
+
+HEADER = os.path.join(dwp_build.INCLUDE, "dwp.h")
+A = 0x7F0000000000  # a 16-byte aligned fake device address
+
+# Fake addresses must never reach a real GPU: every case below is rejected by
+# host validation, but a wrong expectation would hand one to the CUDA runtime.
+pytestmark = pytest.mark.skipif(
+    __import__("torch").cuda.is_available(),
+    reason="host-validation tests use fake device addresses; run them without a GPU")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    dwp_build.build()
+    return dwp.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(dwp_\w+)\s*\(", text, re.M)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert names, "no declarations parsed"
+    assert sorted(dwp.EXPORTS) == names
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+def test_version_and_status_strings(lib):
+    assert dwp.dwp_version() >= 100
+    for code in range(9):
+        s = dwp.dwp_status_string(code)
+        assert s.startswith("DWP_") and "UNKNOWN" not in s
+    assert "UNKNOWN" in dwp.dwp_status_string(99)
+
+
+def test_scan_size_query(lib):
+    tile = None
+    for n in (0, 1, 5, 1 << 20, (1 << 28), (1 << 32) - 1):
+        for entry in (dwp.dwp_scan_exclusive, dwp.dwp_scan_inclusive):
+            st, b = entry(dwp.DWP_U32_ADD, 0, 0, n, 0, 0, 0)
+            assert st == dwp.DWP_SUCCESS
+            assert b >= 128 and (b - 128) % 8 == 0
+            tiles = (b - 128) // 8
+            if n == 0:
+                assert tiles == 0
+            else:
+                if tile is None:
+                    tile = n if n > 1 else None
+                assert tiles >= 1
+    # tiles grow linearly with n
+    _, b1 = dwp.dwp_scan_exclusive(dwp.DWP_U32_ADD, 0, 0, 1 << 24, 0, 0, 0)
+    _, b2 = dwp.dwp_scan_exclusive(dwp.DWP_U32_ADD, 0, 0, 1 << 25, 0, 0, 0)
+    assert (b2 - 128) == 2 * (b1 - 128)
+
+
+def test_scan_validation(lib):
+    E = dwp.dwp_scan_exclusive
+    n = 1000
+    _, need = E(dwp.DWP_U32_ADD, 0, 0, n, 0, 0, 0)
+    scratch = A + (1 << 30)
+    # unknown op, n too large
+    assert E(7, A, A + 8192, n, scratch, need, 0)[0] == dwp.DWP_ERR_INVALID_VALUE
+    assert E(-1, A, A + 8192, n, scratch, need, 0)[0] == dwp.DWP_ERR_INVALID_VALUE
+    assert E(dwp.DWP_U32_ADD, A, A + 8192, 1 << 32, scratch, need, 0)[0] == dwp.DWP_ERR_INVALID_VALUE
+    # scratch too small
+    assert E(dwp.DWP_U32_ADD, A, A + 8192, n, scratch, need - 1, 0)[0] == dwp.DWP_ERR_SCRATCH_TOO_SMALL
+    # null data pointers with n > 0
+    assert E(dwp.DWP_U32_ADD, 0, A, n, scratch, need, 0)[0] == dwp.DWP_ERR_INVALID_VALUE
+    assert E(dwp.DWP_U32_ADD, A, 0, n, scratch, need, 0)[0] == dwp.DWP_ERR_INVALID_VALUE
+    # misaligned pointers
+    assert E(dwp.DWP_U32_ADD, A + 4, A + 8192, n, scratch, need, 0)[0] == dwp.DWP_ERR_MISALIGNED
+    assert E(dwp.DWP_U32_ADD, A, A + 8200, n, scratch, need, 0)[0] == dwp.DWP_ERR_MISALIGNED
+    assert E(dwp.DWP_U32_ADD, A, A + 8192, n, scratch + 8, need, 0)[0] == dwp.DWP_ERR_MISALIGNED
+    # partial overlap of in and out; scratch overlapping data
+    assert E(dwp.DWP_U32_ADD, A, A + 16, n, scratch, need, 0)[0] == dwp.DWP_ERR_ALIASING
+    assert E(dwp.DWP_U32_ADD, A, A + 8192, n, A + 3008, need, 0)[0] == dwp.DWP_ERR_ALIASING
+    assert E(dwp.DWP_U32_ADD, A, A + 8192, n, A + 8192 + 16, need, 0)[0] == dwp.DWP_ERR_ALIASING
+
+
+def test_null_scratch_bytes_pointer(lib):
+    import ctypes
+    st = lib.dwp_scan_exclusive(0, None, None, 10, None, ctypes.POINTER(ctypes.c_size_t)(), None)
+    assert st == dwp.DWP_ERR_INVALID_VALUE
+    assert lib.dwp_read_status(None, None) == dwp.DWP_ERR_INVALID_VALUE
