@@ -1,7 +1,7 @@
-// Device building blocks shared by the scan, segmented-scan and compaction
-// kernels: sm_103a inline PTX for mbarriers, bulk (TMA) copies, proxy fences
-// and acquire/release descriptor traffic; the associative operators; the
-// warp and block scan layers; and the warp-parallel decoupled look-back.
+// Device building blocks shared by the kernels: sm_103a inline PTX for
+// mbarriers, bulk (TMA) copies, proxy fences and descriptor traffic; the
+// associative operators; the warp layer; and the warp-parallel decoupled
+// look-back.
 #pragma once
 
 #include <cstdint>
@@ -10,34 +10,63 @@
 
 namespace dwp {
 
+constexpr uint32_t kNoTile = 0xffffffffu;
+
 // ---------------------------------------------------------------------------
 // Operators.  "Parallel Prefix Sum (Scan), in depth", "Inclusive, exclusive
 // and associative": any associative operator; "Prefix scans and compaction",
 // "Inclusive and exclusive scan": identities 0 for addition, lowest value for
 // a maximum.  combine(a, b) keeps operand order: a covers earlier elements.
+// warp_reduce combines one value per lane over the whole warp.
 
 struct OpU32Add {
+    static constexpr bool kCommutative = true;
     using T = uint32_t;
     static __device__ __forceinline__ T identity() { return 0u; }
     static __device__ __forceinline__ T combine(T a, T b) { return a + b; }
     static __device__ __forceinline__ uint32_t to_bits(T v) { return v; }
     static __device__ __forceinline__ T from_bits(uint32_t b) { return b; }
+    // one redux instruction; `scratch` unused
+    static __device__ __forceinline__ T warp_reduce(T v, uint32_t, uint32_t *) {
+        return __reduce_add_sync(0xffffffffu, v);
+    }
 };
 
 struct OpU32Max {
+    static constexpr bool kCommutative = true;
     using T = uint32_t;
     static __device__ __forceinline__ T identity() { return 0u; }
     static __device__ __forceinline__ T combine(T a, T b) { return a > b ? a : b; }
     static __device__ __forceinline__ uint32_t to_bits(T v) { return v; }
     static __device__ __forceinline__ T from_bits(uint32_t b) { return b; }
+    static __device__ __forceinline__ T warp_reduce(T v, uint32_t, uint32_t *) {
+        return __reduce_max_sync(0xffffffffu, v);
+    }
 };
 
 struct OpF32Add {
+    static constexpr bool kCommutative = true;  // a + b == b + a exactly in IEEE
     using T = float;
     static __device__ __forceinline__ T identity() { return 0.0f; }
     static __device__ __forceinline__ T combine(T a, T b) { return __fadd_rn(a, b); }
     static __device__ __forceinline__ uint32_t to_bits(T v) { return __float_as_uint(v); }
     static __device__ __forceinline__ T from_bits(uint32_t b) { return __uint_as_float(b); }
+    // No float redux instruction: one lane adds the 32 values through a
+    // 33-word shared-memory scratch owned by the calling warp.
+    static __device__ __forceinline__ T warp_reduce(T v, uint32_t lane, uint32_t *scratch) {
+        scratch[lane] = __float_as_uint(v);
+        __syncwarp();
+        if (lane == 0) {
+            float acc = 0.0f;
+#pragma unroll
+            for (int l = 0; l < 32; ++l) acc = __fadd_rn(acc, __uint_as_float(scratch[l]));
+            scratch[32] = __float_as_uint(acc);
+        }
+        __syncwarp();
+        const float r = __uint_as_float(scratch[32]);
+        __syncwarp();
+        return r;
+    }
 };
 
 // ---------------------------------------------------------------------------
@@ -127,26 +156,27 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Barrier among the `nthreads` threads (a multiple of 32) that use `id`.
-__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t nthreads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+// Descriptor publication: one 64-bit device-scope atomic store of state and
+// value together ("Single-Pass Prefix Scan with Decoupled Look-Back", "The
+// publication protocol in code": device scope suffices, and because flag
+// and payload travel in one word a reader can never see one without the
+// other, so the word itself needs no fence).  The store is relaxed, not
+// release: no reader consumes any other memory on the strength of the flag,
+// and a release store (a full fence before it) was measured at about 0.8 us
+// on GB300, on the serial path of every tile.
+__device__ __forceinline__ void st_relaxed_gpu(uint64_t *p, uint64_t v) {
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
-// Descriptor publication and reading: one 64-bit word, release store and
-// acquire load at device (.gpu) scope ("Single-Pass Prefix Scan with
-// Decoupled Look-Back", "The publication protocol in code": device scope
-// suffices; the reader loads the whole word so flag and value never mix).
-__device__ __forceinline__ void st_release_gpu(uint64_t *p, uint64_t v) {
-    asm volatile("st.release.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-
-__device__ __forceinline__ uint64_t ld_acquire_gpu(const uint64_t *p) {
+// Device-scope atomic (relaxed) read of a descriptor word; never hoisted out
+// of a polling loop ("Where the algorithm meets the hardware").
+__device__ __forceinline__ uint64_t ld_relaxed_gpu(const uint64_t *p) {
     uint64_t v;
-    asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
 
-// Plain (non-acquire) volatile read of a shared-memory word.
+// Volatile read of a shared-memory word.
 __device__ __forceinline__ uint32_t ld_volatile_smem(const uint32_t *p) {
     return *reinterpret_cast<const volatile uint32_t *>(p);
 }
@@ -171,74 +201,80 @@ __device__ __forceinline__ uint32_t desc_state(uint64_t d) { return static_cast<
 __device__ __forceinline__ uint32_t desc_bits(uint64_t d) { return static_cast<uint32_t>(d); }
 
 // ---------------------------------------------------------------------------
-// Warp layer: Hillis-Steele inclusive scan over the 32 lanes ("Parallel
-// Prefix Sum (Scan), in depth", "Hillis-Steele: short span, too much work"
-// and "A CUDA scan: warp, block, grid"): at distance d every lane >= d
-// combines the value d lanes below it.
-
-template <class Op>
-__device__ __forceinline__ typename Op::T warp_inclusive_scan(typename Op::T v, uint32_t lane) {
-#pragma unroll
-    for (uint32_t d = 1; d < 32; d <<= 1) {
-        typename Op::T other = __shfl_up_sync(0xffffffffu, v, d);
-        if (lane >= d) v = Op::combine(other, v);
-    }
-    return v;
-}
-
-// ---------------------------------------------------------------------------
 // Decoupled look-back, warp-parallel ("Single-Pass Prefix Scan with
 // Decoupled Look-Back", "Three states in a per-block descriptor" and "Why
 // the work stays linear"; "Parallel Prefix Sum (Scan), in depth", "Scanning
 // a whole array: three grid strategies").
 //
-// Called by all 32 lanes of one warp for tile t > 0.  Lane l reads the
-// descriptor of tile (base - l), so one round covers 32 predecessors.  The
-// round is used once no lane nearer than the nearest terminal (prefix or
-// poison) descriptor is still invalid; the values of the lanes up to and
-// including that terminal lane are combined in tile order and folded in
-// front of the running carry.  Without a terminal lane the window moves 32
-// tiles back.  Returns the exclusive prefix of tile t in *carry_out.
-// Result codes: 0 ok, 1 poison found, 2 spin limit reached.
+// Called by all 32 lanes of one warp for tile t > 0.  One round reads the
+// K*32 nearest unread predecessors at once: position p = 32*i + lane is tile
+// base - p, so a lane's K loads are independent and in flight together.  Two
+// warp-wide min-reductions find the nearest terminal descriptor (prefix or
+// poison) and the nearest invalid one; the round is used once nothing nearer
+// than the terminal one is still invalid (invalid ones are re-polled).  The
+// values up to and including the terminal descriptor are then combined and
+// folded into the carry; without a terminal descriptor the window moves K*32
+// tiles back.  Every plain-scan operator here is commutative (u32 add, u32
+// max, and f32 add, whose a+b == b+a exactly), so values are combined per
+// lane first and then across lanes; for f32 only the grouping changes, the
+// run-to-run variation the method has anyway ("When not to use it").
+// Warp collectives are kept to a few per poll: on a GB300 streaming at full
+// bandwidth each one was measured at several hundred cycles.
+//
+// Returns 0 and the exclusive prefix of tile t in *carry_out; 1 if the
+// nearest terminal descriptor is poison; 2 if the poll limit ran out.
 
-template <class Op>
+template <class Op, int K>
 __device__ __forceinline__ int lookback(const uint64_t *desc, uint32_t t, uint32_t lane,
-                                        uint32_t spin_limit, typename Op::T *carry_out) {
+                                        uint32_t spin_limit, uint32_t *scratch,
+                                        typename Op::T *carry_out) {
     using T = typename Op::T;
+    static_assert(Op::kCommutative, "the look-back combines per lane first");
+    static_assert(K * 32 < (1 << 30), "window positions must fit the key");
     T carry = Op::identity();
     int64_t base = static_cast<int64_t>(t) - 1;
     uint32_t polls = 0;
     while (true) {
-        const int64_t idx = base - static_cast<int64_t>(lane);
-        uint64_t d;
-        uint32_t term_mask, first;
-        while (true) {
-            d = (idx >= 0) ? ld_acquire_gpu(desc + idx) : make_desc(kPrefix, Op::to_bits(Op::identity()));
-            const uint32_t st = desc_state(d);
-            term_mask = __ballot_sync(0xffffffffu, st == kPrefix || st == kPoison);
-            const uint32_t inv_mask = __ballot_sync(0xffffffffu, st == kInvalid);
-            first = term_mask ? (__ffs(term_mask) - 1) : 32u;
-            const uint32_t needed = (first >= 31u) ? 0xffffffffu : ((2u << first) - 1u);
-            if ((inv_mask & needed) == 0u) break;
-            if (++polls >= spin_limit) return 2;
-            if (polls > 4) __nanosleep(polls > 64 ? 256 : 32);
-        }
-        if (first < 32u) {
-            const uint32_t fst = __shfl_sync(0xffffffffu, desc_state(d), first);
-            if (fst == kPoison) return 1;
-        }
-        // Lanes 0..first hold, in reverse tile order, the aggregates and the
-        // terminal prefix; combine them so that earlier tiles stay on the left.
-        T v = (lane <= first) ? Op::from_bits(desc_bits(d)) : Op::identity();
+        uint64_t d[K];
 #pragma unroll
-        for (uint32_t o = 1; o < 32; o <<= 1) {
-            const T earlier = __shfl_down_sync(0xffffffffu, v, o);
-            if (lane + o < 32u) v = Op::combine(earlier, v);
+        for (int i = 0; i < K; ++i) {
+            const int64_t idx = base - 32 * i - static_cast<int64_t>(lane);
+            d[i] = idx >= 0 ? ld_relaxed_gpu(desc + idx)
+                            : make_desc(kPrefix, Op::to_bits(Op::identity()));
         }
-        const T window = __shfl_sync(0xffffffffu, v, 0);
-        carry = Op::combine(window, carry);
-        if (first < 32u) break;
-        base -= 32;
+        uint32_t tkey, imin;
+        while (true) {
+            // key of the nearest terminal descriptor = 2*position + poison bit
+            uint32_t my_t = 0xffffffffu, my_i = 0xffffffffu;
+#pragma unroll
+            for (int i = K - 1; i >= 0; --i) {
+                const uint32_t st = desc_state(d[i]);
+                const uint32_t p = 32u * i + lane;
+                if (st == kPrefix || st == kPoison) my_t = (p << 1) | (st == kPoison ? 1u : 0u);
+                if (st == kInvalid) my_i = p;
+            }
+            tkey = __reduce_min_sync(0xffffffffu, my_t);
+            imin = __reduce_min_sync(0xffffffffu, my_i);
+            if (tkey != 0xffffffffu ? imin > (tkey >> 1) : imin == 0xffffffffu) break;
+            if (++polls >= spin_limit) return 2;
+            if (polls > 8) __nanosleep(polls > 256 ? 256 : 64);
+            const uint32_t lim = tkey != 0xffffffffu ? (tkey >> 1) : 32u * K;
+#pragma unroll
+            for (int i = 0; i < K; ++i) {
+                const int64_t idx = base - 32 * i - static_cast<int64_t>(lane);
+                if (32u * i <= lim && idx >= 0 && desc_state(d[i]) == kInvalid)
+                    d[i] = ld_relaxed_gpu(desc + idx);
+            }
+        }
+        if (tkey != 0xffffffffu && (tkey & 1u)) return 1;
+        const uint32_t last = tkey != 0xffffffffu ? (tkey >> 1) : 0xffffffffu;
+        T acc = Op::identity();
+#pragma unroll
+        for (int i = 0; i < K; ++i)
+            if (32u * i + lane <= last) acc = Op::combine(acc, Op::from_bits(desc_bits(d[i])));
+        carry = Op::combine(Op::warp_reduce(acc, lane, scratch), carry);
+        if (tkey != 0xffffffffu) break;
+        base -= 32 * K;
     }
     *carry_out = carry;
     return 0;
