@@ -46,6 +46,7 @@ EXPORTS = [
     "dwp_status_string",
     "dwp_version",
     "dwp_debug_set_fault",
+    "dwp_scan_static_scratch",
 ]
 
 _lib = None
@@ -81,6 +82,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dwp_version.restype = c.c_int
     lib.dwp_debug_set_fault.argtypes = [c.c_uint32, c.c_uint32]
     lib.dwp_debug_set_fault.restype = c.c_int
+    lib.dwp_scan_static_scratch.argtypes = [c.c_int, c.c_int, P, P, S, P]
+    lib.dwp_scan_static_scratch.restype = c.c_int
     if path == LIB_PATH:
         _lib = lib
     return lib
@@ -105,6 +108,13 @@ def dwp_scan_exclusive(op, d_in, d_out, n, d_scratch, scratch_bytes, stream):
 def dwp_scan_inclusive(op, d_in, d_out, n, d_scratch, scratch_bytes, stream):
     """dwp.h dwp_scan_inclusive; returns (status, scratch_bytes after the call)."""
     return _scan_entry("dwp_scan_inclusive", op, d_in, d_out, n, d_scratch, scratch_bytes, stream)
+
+
+def dwp_scan_static_scratch(op, mode, d_in, d_out, n, stream) -> int:
+    """dwp.h dwp_scan_static_scratch: the scan with the library's built-in
+    scratch, for callers that cannot allocate device memory; returns the status."""
+    return load().dwp_scan_static_scratch(int(op), int(mode), d_in or None, d_out or None, n,
+                                          stream or None)
 
 
 def dwp_read_status(d_scratch, stream) -> int:

@@ -104,6 +104,34 @@ dwp_status dwp_scan_inclusive(dwp_op op, const void *d_in, void *d_out, size_t n
                               void *d_scratch, size_t *scratch_bytes, dwp_stream stream);
 
 /*
+ * Scan for callers that cannot allocate device memory.  The source pages
+ * have no counterpart to this entry point; it is a convenience of this
+ * library.  Code that runs inside another framework's allocator hooks or
+ * memory-pool callbacks (where cudaMalloc would re-enter that allocator),
+ * or a plug-in whose host application owns all device memory, cannot hand
+ * the other scan calls a scratch buffer.  This call uses instead a fixed
+ * array of about 512 KiB that is part of the library's device image: every
+ * GPU that loads libdwp.so holds it until the process exits.  The call
+ * itself allocates and frees nothing.
+ *   op, d_in, d_out, stream: as dwp_scan_exclusive.
+ *   mode      DWP_EXCLUSIVE or DWP_INCLUSIVE.
+ *   n         0 <= n <= DWP_SCAN_STATIC_MAX_N (2^28 elements); a larger n
+ *             returns DWP_ERR_SCRATCH_TOO_SMALL before anything is enqueued.
+ * The first call on a device looks up that device's address of the array
+ * (cudaGetSymbolAddress, with the device current); make that first call
+ * before any stream capture.  Every call on a device shares the one array,
+ * and each call clears the part it uses on `stream` first, so calls must be
+ * ordered on the GPU: two calls that overlap on the GPU (different streams,
+ * not synchronised) race and give wrong results.  Device-side timeouts are
+ * recorded in the array's status word, which dwp_read_status cannot reach:
+ * this entry point does not report them.  DWP_ERR_NO_DEVICE if there is no
+ * current device; otherwise the errors of dwp_scan_exclusive.
+ */
+#define DWP_SCAN_STATIC_MAX_N 268435456u
+dwp_status dwp_scan_static_scratch(dwp_op op, dwp_mode mode, const void *d_in, void *d_out,
+                                   size_t n, dwp_stream stream);
+
+/*
  * Device-side status of the most recent call that used d_scratch.
  * Synchronises `stream`, then reads the status word.  Returns DWP_SUCCESS,
  * DWP_ERR_LOOKBACK_TIMEOUT or DWP_ERR_PIPELINE_TIMEOUT; DWP_ERR_CUDA if the
