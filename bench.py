@@ -200,6 +200,9 @@ def main() -> None:
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=10.0)
+    ap.add_argument("--log2n", type=int, default=28,
+                    help="problem size 2^k (default 28, the benchmarked workload; smaller "
+                         "sizes are for profiler captures)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     args.steps = max(args.steps, 1)
@@ -239,8 +242,9 @@ def main() -> None:
         return float(t.item())
 
     import ctypes
-    n = N_FULL
+    n = 1 << args.log2n
     x_host = torch.from_numpy(synth.u32_full_values(n).view(np.int32)).pin_memory()
+    wl = "u32 exclusive sum scan, n=2^%d, values uniform in [0, 2^32)" % args.log2n
     x = x_host.to(dev)
     y = torch.empty_like(x)
     need = dwp.scan_scratch_bytes(n)
@@ -320,7 +324,7 @@ def main() -> None:
         "vs_baseline": None,
         "dtype": "u32",
         "data": "synthetic (SplitMix64 seed 0xD3B00002, values uniform in [0, 2^32))",
-        "config": {"workload": "u32 exclusive sum scan, n=2^28, values uniform in [0, 2^32)",
+        "config": {"workload": wl,
                    "n": n, "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2 (1 GiB in + 1 GiB out vs 129 MB L2); no flush"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
@@ -354,8 +358,8 @@ def cpu_baseline(x: np.ndarray, budget_s: float) -> dict:
         if runs >= 100:
             break
     return {"value": runs * x.size / t_total / 1e9, "unit": "Gelem/s", "cores": 1, "kind": "oracle",
-            "sample": "%d full passes over the n=2^28 input (%.1f s), sequential C oracle on one host core"
-                      % (runs, t_total)}
+            "sample": "%d full passes over the n=2^%d input (%.1f s), sequential C oracle on one host core"
+                      % (runs, int(x.size).bit_length() - 1, t_total)}
 
 
 def time_calls(fn, steps: int, warmup: int, stream) -> float:

@@ -56,13 +56,13 @@ struct ScanConfig {
 };
 
 #ifndef DWP_SCAN_WARPS
-#define DWP_SCAN_WARPS 8
+#define DWP_SCAN_WARPS 16
 #endif
 #ifndef DWP_SCAN_ITEMS
 #define DWP_SCAN_ITEMS 20
 #endif
 #ifndef DWP_SCAN_STAGES
-#define DWP_SCAN_STAGES 8
+#define DWP_SCAN_STAGES 5
 #endif
 #ifndef DWP_SCAN_LOOKK
 #define DWP_SCAN_LOOKK 4

@@ -60,10 +60,22 @@ def test_scan_size_query(lib):
                 if tile is None:
                     tile = n if n > 1 else None
                 assert tiles >= 1
-    # tiles grow linearly with n
-    _, b1 = dwp.dwp_scan_exclusive(dwp.DWP_U32_ADD, 0, 0, 1 << 24, 0, 0, 0)
-    _, b2 = dwp.dwp_scan_exclusive(dwp.DWP_U32_ADD, 0, 0, 1 << 25, 0, 0, 0)
-    assert (b2 - 128) == 2 * (b1 - 128)
+    # one descriptor per tile: the tile size T is the largest n that needs one
+    _, b1 = dwp.dwp_scan_exclusive(dwp.DWP_U32_ADD, 0, 0, 1, 0, 0, 0)
+    T = 1
+    while dwp.dwp_scan_exclusive(dwp.DWP_U32_ADD, 0, 0, 2 * T, 0, 0, 0)[1] == b1:
+        T *= 2
+    lo, hi = T, 2 * T  # T needs one descriptor, 2T needs two
+    while hi - lo > 1:
+        mid = (lo + hi) // 2
+        if dwp.dwp_scan_exclusive(dwp.DWP_U32_ADD, 0, 0, mid, 0, 0, 0)[1] == b1:
+            lo = mid
+        else:
+            hi = mid
+    T = lo
+    for k in (1, 7, 1000):
+        assert dwp.dwp_scan_exclusive(dwp.DWP_U32_ADD, 0, 0, k * T, 0, 0, 0)[1] == 128 + 8 * k
+        assert dwp.dwp_scan_exclusive(dwp.DWP_U32_ADD, 0, 0, k * T + 1, 0, 0, 0)[1] == 128 + 8 * (k + 1)
 
 
 def test_scan_validation(lib):
