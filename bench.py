@@ -398,7 +398,37 @@ def measure_secondary(dwp, lib, dev, stream, peaks, x, y, scratch, need) -> dict
         gbs = 8 * n / (ms * 1e-3) / 1e9
         out[name] = {"n": n, "ms": ms, "Gelem_s": n / (ms * 1e-3) / 1e9, "GB_s": gbs,
                      "frac": gbs / peaks["hbm_gbs"]}
+    del xf
+    out["segscan_u32_exclusive"] = measure_segscan(dwp, lib, dev, stream, peaks)
     return out
+
+
+def measure_segscan(dwp, lib, dev, stream, peaks) -> dict:
+    """Segmented exclusive u32 scan, n = 2^27 values in [0, 255], Zipf(1.2)
+    segment lengths capped at 2^22 with 5% empty segments (CSR offsets)."""
+    import ctypes
+    import torch
+    n = 1 << 27
+    off_np = synth.segment_offsets(n)
+    nseg = off_np.size - 1
+    v = torch.from_numpy(synth.u32_byte_values(n).view(np.int32)).to(dev)
+    off = torch.from_numpy(off_np.view(np.int32)).to(dev)
+    y = torch.empty_like(v)
+    need = dwp.segmented_scan_scratch_bytes(n)
+    scratch = dwp.alloc_scratch(need, dev)
+    sb = ctypes.c_size_t(need)
+    args = (ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(off.data_ptr()), nseg,
+            ctypes.c_void_p(y.data_ptr()), n, dwp.DWP_EXCLUSIVE, ctypes.c_void_p(scratch.data_ptr()),
+            ctypes.byref(sb), ctypes.c_void_p(int(stream.cuda_stream)))
+    ms = time_calls(lambda: lib.dwp_segmented_scan_u32(*args), 200, 5, stream)
+    if dwp.read_status(scratch) != dwp.DWP_SUCCESS:
+        raise RuntimeError("segmented scan reported a device-side error")
+    alg = 8 * n + 4 * (nseg + 1)
+    gbs = alg / (ms * 1e-3) / 1e9
+    return {"n": n, "segments": nseg, "ms": ms, "Gelem_s": n / (ms * 1e-3) / 1e9, "GB_s": gbs,
+            "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": alg,
+            "workload": "segmented exclusive u32 sum scan, n=2^27 values in [0,255], Zipf(1.2) "
+                        "lengths capped at 2^22, 5% empty, CSR offsets (SplitMix64 seed 0xD3B00005)"}
 
 
 if __name__ == "__main__":

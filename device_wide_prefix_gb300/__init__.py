@@ -42,6 +42,7 @@ DWP_INCLUSIVE = 1
 EXPORTS = [
     "dwp_scan_exclusive",
     "dwp_scan_inclusive",
+    "dwp_segmented_scan_u32",
     "dwp_read_status",
     "dwp_status_string",
     "dwp_version",
@@ -74,6 +75,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         f = getattr(lib, name)
         f.argtypes = [c.c_int, P, P, S, P, Z, P]
         f.restype = c.c_int
+    lib.dwp_segmented_scan_u32.argtypes = [P, P, S, P, S, c.c_int, P, Z, P]
+    lib.dwp_segmented_scan_u32.restype = c.c_int
     lib.dwp_read_status.argtypes = [P, P]
     lib.dwp_read_status.restype = c.c_int
     lib.dwp_status_string.argtypes = [c.c_int]
@@ -108,6 +111,16 @@ def dwp_scan_exclusive(op, d_in, d_out, n, d_scratch, scratch_bytes, stream):
 def dwp_scan_inclusive(op, d_in, d_out, n, d_scratch, scratch_bytes, stream):
     """dwp.h dwp_scan_inclusive; returns (status, scratch_bytes after the call)."""
     return _scan_entry("dwp_scan_inclusive", op, d_in, d_out, n, d_scratch, scratch_bytes, stream)
+
+
+def dwp_segmented_scan_u32(d_values, d_offsets, num_segments, d_out, n, mode, d_scratch,
+                           scratch_bytes, stream):
+    """dwp.h dwp_segmented_scan_u32; returns (status, scratch_bytes after the call)."""
+    sb = ctypes.c_size_t(scratch_bytes)
+    st = load().dwp_segmented_scan_u32(d_values or None, d_offsets or None, num_segments,
+                                       d_out or None, n, int(mode), d_scratch or None,
+                                       ctypes.byref(sb), stream or None)
+    return st, sb.value
 
 
 def dwp_scan_static_scratch(op, mode, d_in, d_out, n, stream) -> int:
@@ -206,6 +219,38 @@ def scan_exclusive(x, op: str = "u32_add", out=None, scratch=None, stream=None):
 def scan_inclusive(x, op: str = "u32_add", out=None, scratch=None, stream=None):
     """Inclusive scan of a contiguous CUDA tensor (int32/uint32 bits or float32)."""
     return _scan(True, x, op, out, scratch, stream)
+
+
+def segmented_scan_scratch_bytes(n: int) -> int:
+    st, b = dwp_segmented_scan_u32(None, None, 0, None, n, DWP_EXCLUSIVE, None, 0, None)
+    _check(st, "segmented scan scratch size query")
+    return b
+
+
+def segmented_scan(values, offsets, inclusive: bool = False, out=None, scratch=None,
+                   stream=None):
+    """Segmented u32 scan of `values` (CUDA int32/uint32 bits) over CSR `offsets`
+    (CUDA, N+1 entries).  Rows outside [offsets[0], offsets[N]) keep the
+    contents of `out` (uninitialised when `out` is None)."""
+    torch = _torch()
+    if not (values.is_cuda and offsets.is_cuda and values.is_contiguous() and offsets.is_contiguous()):
+        raise ValueError("values and offsets must be contiguous CUDA tensors")
+    if values.element_size() != 4 or offsets.element_size() != 4:
+        raise ValueError("values and offsets must have 4-byte elements")
+    n = values.numel()
+    nseg = max(offsets.numel() - 1, 0)
+    if out is None:
+        out = torch.empty_like(values)
+    need = segmented_scan_scratch_bytes(n)
+    if scratch is None:
+        scratch = alloc_scratch(need, values.device)
+    with torch.cuda.device(values.device):
+        st, _ = dwp_segmented_scan_u32(values.data_ptr(), offsets.data_ptr() if offsets.numel() else 0,
+                                       nseg, out.data_ptr(), n,
+                                       DWP_INCLUSIVE if inclusive else DWP_EXCLUSIVE,
+                                       scratch.data_ptr(), scratch.numel(), _stream_of(values, stream))
+    _check(st, "dwp_segmented_scan_u32")
+    return out
 
 
 def read_status(scratch, stream=None) -> int:

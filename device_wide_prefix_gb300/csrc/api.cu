@@ -58,9 +58,57 @@ dwp_status scan_common(bool inclusive, dwp_op op, const void *in, void *out, siz
     return DWP_SUCCESS;
 }
 
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+dwp_status segscan_common(const uint32_t *values, const uint32_t *offsets, size_t nseg,
+                          uint32_t *out, size_t n, dwp_mode mode, void *scratch,
+                          size_t *scratch_bytes, dwp_stream stream) {
+    if (!scratch_bytes) return DWP_ERR_INVALID_VALUE;
+    const int m = static_cast<int>(mode);
+    if (m != DWP_EXCLUSIVE && m != DWP_INCLUSIVE) return DWP_ERR_INVALID_VALUE;
+    if (uint64_t(n) > kMaxN || uint64_t(nseg) >= kMaxN) return DWP_ERR_INVALID_VALUE;
+    const uint64_t tiles = ceil_div(n, segscan_tile_elems());
+    const size_t need = scratch_bytes_for_tiles(tiles);
+    if (!scratch) {
+        *scratch_bytes = need;
+        return DWP_SUCCESS;
+    }
+    if (*scratch_bytes < need) return DWP_ERR_SCRATCH_TOO_SMALL;
+    if (n > 0 && (!values || !out)) return DWP_ERR_INVALID_VALUE;
+    if (!offsets && (nseg > 0 || n > 0)) return DWP_ERR_INVALID_VALUE;
+    if (!aligned16(scratch) || (n > 0 && (!aligned16(values) || !aligned16(out))) ||
+        (offsets && !aligned4(offsets)))
+        return DWP_ERR_MISALIGNED;
+    const uint64_t bytes = uint64_t(n) * 4u, obytes = (uint64_t(nseg) + 1u) * 4u;
+    if (overlap(out, bytes, values, bytes) || overlap(out, bytes, offsets, obytes) ||
+        overlap(scratch, need, values, bytes) || overlap(scratch, need, offsets, obytes) ||
+        overlap(scratch, need, out, bytes))
+        return DWP_ERR_ALIASING;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(scratch, 0, need, s) != cudaSuccess) {
+        cudaGetLastError();
+        return DWP_ERR_CUDA;
+    }
+    if (n == 0 || nseg == 0) return DWP_SUCCESS;  // no row lies in a segment
+    if (launch_segscan(values, offsets, uint32_t(nseg), out, n, m == DWP_INCLUSIVE, scratch, s) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return DWP_ERR_CUDA;
+    }
+    return DWP_SUCCESS;
+}
+
 }  // namespace
 
 extern "C" {
+
+dwp_status dwp_segmented_scan_u32(const uint32_t *d_values, const uint32_t *d_offsets,
+                                  size_t num_segments, uint32_t *d_out, size_t n, dwp_mode mode,
+                                  void *d_scratch, size_t *scratch_bytes, dwp_stream stream) {
+    return segscan_common(d_values, d_offsets, num_segments, d_out, n, mode, d_scratch,
+                          scratch_bytes, stream);
+}
 
 dwp_status dwp_scan_exclusive(dwp_op op, const void *d_in, void *d_out, size_t n,
                               void *d_scratch, size_t *scratch_bytes, dwp_stream stream) {

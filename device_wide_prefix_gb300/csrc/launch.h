@@ -19,4 +19,11 @@ uint32_t scan_tile_elems();
 cudaError_t launch_scan(dwp_op op, bool inclusive, const void *in, void *out, uint64_t n,
                         void *scratch, cudaStream_t stream);
 
+// Elements per tile of the segmented scan kernel.
+uint32_t segscan_tile_elems();
+// One launch of the segmented u32 scan (scratch already cleared; nseg >= 1).
+cudaError_t launch_segscan(const uint32_t *values, const uint32_t *offsets, uint32_t nseg,
+                           uint32_t *out, uint64_t n, bool inclusive, void *scratch,
+                           cudaStream_t stream);
+
 }  // namespace dwp

@@ -1,0 +1,533 @@
+// Segmented u32 addition scan over CSR offsets, single pass with decoupled
+// look-back, for sm_103a.
+//
+// "GPUSegmentedScan" (luma.gl), sections "Prefix scans and segmented scans"
+// and "Contract": segment s is rows [offsets[s], offsets[s+1]); the running
+// total restarts at every segment; empty segments write nothing.  "Parallel
+// Prefix Sum (Scan), in depth", section "What scan builds": a segmented scan
+// carries a flag with each value, i.e. it scans (head, value) pairs with
+//     (h1, v1) (+) (h2, v2) = (h1 | h2, h2 ? v2 : v1 + v2),
+// an associative, non-commutative operator.
+//
+// The pipeline is the plain scan's (scan.cu): producer warp with bulk loads
+// into a ring of stages, one tile warp per stage, consumer warps with
+// per-warp bulk stores.  What differs:
+//   * the tile warp first marks the heads of its tile (every offset value in
+//     [tile start, tile end)) in a shared-memory bitmap.  It finds the first
+//     offset at or after the tile start in a per-block sample of the offsets
+//     held in shared memory (exact when N + 1 <= kSample, the skewed-length
+//     workload's case), else by a warp-wide 32-ary search of global memory
+//     inside the sampled interval; then it walks the offsets of the tile;
+//   * per-thread totals and their exclusive prefix are (head, value) pairs;
+//   * a tile holding a head publishes its inclusive prefix at once (its value
+//     after its last head is final); the look-back then is a plain u32-add
+//     look-back that stops at the nearest prefix, and runs only if the
+//     tile's first row is not itself a head;
+//   * rows outside [offsets[0], min(offsets[N], n)) are not written.
+// Offsets are trusted (no readback, "Limitations"): unordered offsets give
+// unspecified values but every access stays inside offsets[0..N].
+#include <cuda_runtime.h>
+
+#include "device.cuh"
+#include "launch.h"
+
+namespace dwp {
+
+namespace {
+
+constexpr int kSample = 2048;  // offsets sampled into shared memory per block
+
+template <int NW_, int ITEMS_, int STAGES_, int LOOKK_>
+struct SegConfig {
+    static constexpr int kWarps = NW_;
+    static constexpr int kItems = ITEMS_;
+    static constexpr int kStages = STAGES_;
+    static constexpr int kLookK = LOOKK_;
+    static constexpr int kThreads = (1 + STAGES_ + NW_) * 32;
+    static constexpr int kConsumers = NW_ * 32;
+    static constexpr int kWarpElems = 32 * ITEMS_;
+    static constexpr int kTile = NW_ * 32 * ITEMS_;
+    static_assert(ITEMS_ % 4 == 0 && (ITEMS_ / 4) % 2 == 1, "ITEMS must be an odd multiple of 4");
+    static_assert(ITEMS_ <= 32, "a thread's head bits span at most two bitmap words");
+    static_assert(NW_ >= 1 && NW_ <= 32, "");
+    static constexpr size_t kStageBytes = size_t(kTile) * 4;
+    static constexpr int kPrefixWords = kConsumers + kConsumers / 8;
+    static constexpr int kHeadWords = kTile / 32 + 1;   // tile head bitmap (+1 spill word)
+    static constexpr int kPHeadWords = kConsumers / 4;   // one head byte per consumer thread
+    // mbarriers 32 B; tile id, carry, look-back result, pad 16 B; prefixes;
+    // prefix head bits; tile head bitmap; lane totals 33 + lane head bits 33
+    static constexpr size_t kStageMeta =
+        48 + 4 * (kPrefixWords + kPHeadWords + kHeadWords + 66 + 33);
+    // + abort, end, lo, hi words + the offset sample
+    static constexpr size_t kSmemBytes = (kStageBytes + kStageMeta) * kStages + 16 + 4 * kSample;
+};
+
+#ifndef DWP_SEG_WARPS
+#define DWP_SEG_WARPS 16
+#endif
+#ifndef DWP_SEG_ITEMS
+#define DWP_SEG_ITEMS 20
+#endif
+#ifndef DWP_SEG_STAGES
+#define DWP_SEG_STAGES 4
+#endif
+using SegCfg = SegConfig<DWP_SEG_WARPS, DWP_SEG_ITEMS, DWP_SEG_STAGES, 4>;
+
+template <class C>
+struct SegSmem {
+    unsigned char *base;
+    __device__ explicit SegSmem(unsigned char *p) : base(p) {}
+    __device__ uint32_t *data(int s) const {
+        return reinterpret_cast<uint32_t *>(base + size_t(s) * C::kStageBytes);
+    }
+    __device__ unsigned char *meta(int s) const {
+        return base + C::kStageBytes * C::kStages + size_t(s) * C::kStageMeta;
+    }
+    __device__ uint64_t *full(int s) const { return reinterpret_cast<uint64_t *>(meta(s)); }
+    __device__ uint64_t *carry_ready(int s) const { return full(s) + 1; }
+    __device__ uint64_t *empty(int s) const { return full(s) + 2; }
+    __device__ uint32_t *tile_id(int s) const { return reinterpret_cast<uint32_t *>(meta(s) + 32); }
+    __device__ uint32_t *carry(int s) const { return tile_id(s) + 1; }
+    __device__ uint32_t *lbres(int s) const { return tile_id(s) + 2; }
+    __device__ uint32_t *prefix(int s) const { return tile_id(s) + 4; }
+    __device__ unsigned char *phead(int s) const {
+        return reinterpret_cast<unsigned char *>(prefix(s) + C::kPrefixWords);
+    }
+    __device__ uint32_t *heads(int s) const { return prefix(s) + C::kPrefixWords + C::kPHeadWords; }
+    __device__ uint32_t *lane_tot(int s) const { return heads(s) + C::kHeadWords; }
+    __device__ uint32_t *lane_head(int s) const { return lane_tot(s) + 33; }
+    __device__ uint32_t *lb_scratch(int s) const { return lane_head(s) + 33; }
+    __device__ uint32_t *words() const {
+        return reinterpret_cast<uint32_t *>(base + (C::kStageBytes + C::kStageMeta) * C::kStages);
+    }
+    __device__ uint32_t *abort_flag() const { return words(); }
+    __device__ uint32_t *end_iter() const { return words() + 1; }
+    __device__ uint32_t *cover_lo() const { return words() + 2; }
+    __device__ uint32_t *cover_hi() const { return words() + 3; }
+    __device__ uint32_t *sample() const { return words() + 4; }
+};
+
+__device__ __forceinline__ uint32_t prefix_slot(uint32_t c) { return c + (c >> 3); }
+
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, kPipeWaitLimit));
+}
+
+__device__ __forceinline__ int warp_wait_or_end(uint64_t *bar, uint32_t parity, uint32_t k,
+                                                const uint32_t *end_iter) {
+    uint32_t r = 0;
+    for (uint32_t i = 0; i < kPipeWaitLimit; ++i) {
+        if (mbar_try_wait(bar, parity)) {
+            r = 2;
+            break;
+        }
+        if (ld_volatile_smem(end_iter) < k) {
+            r = 1;
+            break;
+        }
+        if (i >= 8) __nanosleep(64);
+    }
+    return int(__reduce_max_sync(0xffffffffu, r));
+}
+
+__device__ __forceinline__ uint32_t seg_elem(const uint32_t *buf, const uint32_t *in, uint64_t base,
+                                             uint32_t pos, uint32_t bulk, uint32_t valid) {
+    if (pos < bulk) return buf[pos];
+    if (pos < valid) return in[base + pos];
+    return 0u;
+}
+
+// Head bits [pos, pos + cnt) of a tile bitmap, cnt <= 32, as the low bits.
+__device__ __forceinline__ uint32_t head_bits(const uint32_t *heads, uint32_t pos, uint32_t cnt) {
+    const uint32_t w = pos >> 5, b = pos & 31u;
+    uint64_t v = (uint64_t(heads[w + 1]) << 32) | heads[w];
+    v >>= b;
+    return cnt >= 32 ? uint32_t(v) : uint32_t(v) & ((1u << cnt) - 1u);
+}
+
+// Warp-wide: the first index k in [lo, hi] with off[k] >= key, given that
+// off[lo-1] < key (or lo == 0) and that hi is a valid answer (off[hi] >= key,
+// or hi == N + 1).  Each round probes 32 evenly spaced indices below hi and
+// keeps the sub-interval between the last probe below the key and the first
+// one at or above it; probes stay inside [lo, hi), so inside offsets[0..N].
+__device__ __forceinline__ uint32_t warp_lower_bound(const uint32_t *off, uint32_t lo, uint32_t hi,
+                                                     uint32_t key, uint32_t lane) {
+    while (lo < hi) {
+        const uint32_t len = hi - lo;
+        const uint32_t step = (len + 31u) / 32u;
+        const uint64_t q = uint64_t(lo) + uint64_t(lane + 1u) * step - 1u;
+        const bool probe = q < hi;
+        const bool below = probe && __ldg(off + q) < key;
+        const uint32_t c = __reduce_add_sync(0xffffffffu, below ? 1u : 0u);
+        const uint32_t np = __reduce_add_sync(0xffffffffu, probe ? 1u : 0u);
+        if (c < np) hi = lo + (c + 1u) * step - 1u;  // probe c is at or above the key
+        lo = lo + c * step;                          // probes 0 .. c-1 are below it
+    }
+    return lo;
+}
+
+template <bool INCL, class C>
+__global__ void __launch_bounds__(C::kThreads, 1)
+    segscan_kernel(const uint32_t *in, const uint32_t *off, uint32_t nseg, uint32_t *out,
+                   uint64_t n, uint32_t num_tiles, ScratchHeader *hdr, uint64_t *desc,
+                   FaultConfig fault) {
+    using Op = OpU32Add;
+    constexpr int NW = C::kWarps, ITEMS = C::kItems, STAGES = C::kStages, TILE = C::kTile;
+    constexpr int WE = C::kWarpElems;
+    constexpr uint32_t NCONS = C::kConsumers;
+
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    const SegSmem<C> sm(smem_raw);
+    const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
+
+    // offset sample: sample[i] = off[min(i * stride, N)]
+    const uint64_t noff = uint64_t(nseg) + 1;
+    const uint32_t stride = uint32_t((noff + kSample - 1) / kSample);
+    const uint32_t nsample = uint32_t((noff + stride - 1) / stride);
+    for (uint32_t i = threadIdx.x; i < nsample; i += blockDim.x)
+        sm.sample()[i] = __ldg(off + min(uint64_t(i) * stride, uint64_t(nseg)));
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(sm.full(s), 1);
+            mbar_init(sm.carry_ready(s), 1);
+            mbar_init(sm.empty(s), NW);
+        }
+        *sm.abort_flag() = 0;
+        *sm.end_iter() = kNoTile;
+        const uint32_t lo = __ldg(off), last = __ldg(off + nseg);
+        *sm.cover_lo() = lo;
+        *sm.cover_hi() = uint32_t(min(uint64_t(last), n));
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    auto tile_extent = [&](uint32_t t, uint32_t &valid, uint32_t &bulk) {
+        const uint64_t rem = n - uint64_t(t) * TILE;
+        valid = rem < uint64_t(TILE) ? uint32_t(rem) : uint32_t(TILE);
+        bulk = valid == uint32_t(TILE) ? valid : (valid & ~3u);
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------- producer
+        if (lane != 0) return;
+        for (uint32_t k = 0;; ++k) {
+            const int s = int(k % STAGES);
+            if (k >= STAGES && !mbar_wait(sm.empty(s), ((k / STAGES) - 1) & 1u, kPipeWaitLimit)) {
+                record_error(hdr, DWP_ERR_PIPELINE_TIMEOUT);
+                *reinterpret_cast<volatile uint32_t *>(sm.end_iter()) = k - 1;
+                return;
+            }
+            uint32_t t = kNoTile;
+            if (ld_volatile_smem(sm.abort_flag()) == 0) {
+                t = atomicAdd(&hdr->tile_counter, 1u);
+                if (t >= num_tiles) t = kNoTile;
+            }
+            *reinterpret_cast<volatile uint32_t *>(sm.tile_id(s)) = t;
+            if (t == kNoTile) {
+                *reinterpret_cast<volatile uint32_t *>(sm.end_iter()) = k;
+                mbar_arrive(sm.full(s));
+                return;
+            }
+            uint32_t valid, bulk;
+            tile_extent(t, valid, bulk);
+            if (bulk) {
+                mbar_arrive_expect_tx(sm.full(s), bulk * 4u);
+                bulk_load(sm.data(s), in + uint64_t(t) * TILE, bulk * 4u, sm.full(s));
+            } else {
+                mbar_arrive(sm.full(s));
+            }
+        }
+    }
+
+    if (warp <= uint32_t(STAGES)) {
+        // ----------------------------------------------------- tile warps
+        const int s = int(warp) - 1;
+        bool draining = false;
+        for (uint32_t use = 0;; ++use) {
+            const int w = warp_wait_or_end(sm.full(s), use & 1u, use * STAGES + uint32_t(s),
+                                           sm.end_iter());
+            if (w != 2) {
+                if (w == 0 && lane == 0) record_error(hdr, DWP_ERR_PIPELINE_TIMEOUT);
+                return;
+            }
+            const uint32_t t = ld_volatile_smem(sm.tile_id(s));
+            if (t == kNoTile) {
+                if (lane == 0) mbar_arrive(sm.carry_ready(s));
+                return;
+            }
+            if (!draining && ld_volatile_smem(sm.abort_flag()) != 0) draining = true;
+            if (draining) {
+                if (lane == 0) {
+                    st_relaxed_gpu(desc + t, make_desc(kPoison, 0u));
+                    *sm.lbres(s) = 1u;
+                    mbar_arrive(sm.carry_ready(s));
+                }
+                __syncwarp();
+                continue;
+            }
+            uint32_t valid, bulk;
+            tile_extent(t, valid, bulk);
+            const uint64_t base = uint64_t(t) * TILE;
+            const uint64_t tend = base + valid;
+            uint32_t *heads = sm.heads(s);
+
+            // -- S1: heads of this tile ------------------------------------
+            for (int i = int(lane); i < C::kHeadWords; i += 32) heads[i] = 0u;
+            __syncwarp();
+            // last sampled offset below the tile start (sample 0 may not be)
+            const uint32_t *smp = sm.sample();
+            uint32_t a = 0, b = nsample;  // first sample >= base, by binary search
+            while (a < b) {
+                const uint32_t m = (a + b) >> 1;
+                if (uint64_t(smp[m]) < base) a = m + 1; else b = m;
+            }
+            uint32_t k0;
+            if (a == 0) {
+                k0 = 0;
+            } else if (stride == 1u) {
+                k0 = a;
+            } else {
+                const uint32_t lo = (a - 1) * stride + 1;
+                const uint32_t hi = uint32_t(min(uint64_t(a) * stride, uint64_t(nseg) + 1));
+                k0 = warp_lower_bound(off, lo, hi, uint32_t(base), lane);
+            }
+            // walk the offsets inside [base, tend)
+            for (uint32_t k = k0; k <= nseg; k += 32) {
+                const uint64_t idx = uint64_t(k) + lane;
+                uint32_t p = 0xffffffffu;
+                if (idx <= nseg) p = stride == 1u ? smp[idx] : __ldg(off + idx);
+                const bool inside = idx <= nseg && uint64_t(p) >= base && uint64_t(p) < tend;
+                if (inside) {
+                    const uint32_t r = uint32_t(uint64_t(p) - base);
+                    atomicOr(&heads[r >> 5], 1u << (r & 31u));
+                }
+                // stop once some offset in this batch reached the tile end
+                if (__any_sync(0xffffffffu, idx > nseg || uint64_t(p) >= tend)) break;
+            }
+            __syncwarp();
+
+            // -- per-thread (head, value) totals ---------------------------
+            const uint32_t *buf = sm.data(s);
+            uint32_t *pre = sm.prefix(s);
+            unsigned char *ph = sm.phead(s);
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                const uint32_t c = lane + 32u * w;
+                const uint32_t hb = head_bits(heads, c * ITEMS, ITEMS);
+                uint32_t acc = 0;
+                if (valid == uint32_t(TILE)) {
+                    const uint4 *v4 = reinterpret_cast<const uint4 *>(buf);
+                    // only the items from the last head on count
+                    const int from = hb ? 31 - __clz(hb) : 0;
+#pragma unroll
+                    for (int v = 0; v < ITEMS / 4; ++v) {
+                        const uint4 q = v4[c * (ITEMS / 4) + v];
+                        const uint32_t qq[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if (4 * v + e >= from) acc += qq[e];
+                    }
+                } else {
+                    for (int j = 0; j < ITEMS; ++j) {
+                        const uint32_t x = seg_elem(buf, in, base, c * ITEMS + j, bulk, valid);
+                        acc = ((hb >> j) & 1u) ? x : acc + x;
+                    }
+                }
+                pre[prefix_slot(c)] = acc;
+                ph[c] = hb ? 1 : 0;
+            }
+            __syncwarp();
+            // lane l scans threads PER*l .. PER*l+PER-1 with the pair operator
+            constexpr int PER = NCONS / 32;
+            uint32_t mv[PER], mh = 0, rv = 0, rh = 0;
+#pragma unroll
+            for (int j = 0; j < PER; ++j) {
+                const uint32_t c = lane * PER + j;
+                mv[j] = rv;
+                if (rh) mh |= 1u << j;
+                const uint32_t hv = ph[c];
+                const uint32_t v = pre[prefix_slot(c)];
+                rv = hv ? v : rv + v;
+                rh |= hv;
+            }
+            sm.lane_tot(s)[lane] = rv;
+            sm.lane_head(s)[lane] = rh;
+            __syncwarp();
+            uint32_t ev = 0, eh = 0, av = 0, ah = 0;  // lane exclusive pair, tile aggregate
+#pragma unroll
+            for (int l = 0; l < 32; ++l) {
+                const uint32_t v = sm.lane_tot(s)[l], h = sm.lane_head(s)[l];
+                if (uint32_t(l) < lane) {
+                    ev = h ? v : ev + v;
+                    eh |= h;
+                }
+                av = h ? v : av + v;
+                ah |= h;
+            }
+            // each thread's exclusive pair: value in pre, head flag in ph
+            // (lane l rewrites only its own PER slots)
+#pragma unroll
+            for (int j = 0; j < PER; ++j) {
+                const uint32_t hj = (mh >> j) & 1u;
+                pre[prefix_slot(lane * PER + j)] = hj ? mv[j] : ev + mv[j];
+                ph[lane * PER + j] = (hj | eh) ? 1 : 0;
+            }
+            __syncwarp();
+            // -- publish, look back ------------------------------------------
+            const bool first_is_head = (heads[0] & 1u) != 0u;
+            if (lane == 0 && t != fault.never_publish_tile)
+                st_relaxed_gpu(desc + t,
+                               make_desc((t == 0 || ah) ? kPrefix : kAggregate, av));
+            uint32_t carry = 0;
+            int rc = 0;
+            if (t != 0 && !first_is_head)
+                rc = lookback<Op, C::kLookK>(desc, t, lane, fault.spin_limit, sm.lb_scratch(s), &carry);
+            if (lane == 0) {
+                if (rc == 0) {
+                    if (t != 0 && !ah && t != fault.never_publish_tile)
+                        st_relaxed_gpu(desc + t, make_desc(kPrefix, carry + av));
+                } else {
+                    st_relaxed_gpu(desc + t, make_desc(kPoison, 0u));
+                    if (rc == 2) record_error(hdr, DWP_ERR_LOOKBACK_TIMEOUT);
+                    *reinterpret_cast<volatile uint32_t *>(sm.abort_flag()) = 1u;
+                }
+                *sm.carry(s) = carry;
+                *sm.lbres(s) = uint32_t(rc);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sm.carry_ready(s));
+            if (rc != 0) draining = true;
+        }
+    }
+
+    // ---------------------------------------------------------- consumers
+    const uint32_t cw = warp - 1 - STAGES;
+    const uint32_t c = cw * 32 + lane;
+    const uint64_t cover_lo = *sm.cover_lo(), cover_hi = *sm.cover_hi();
+    int pending = -1;
+    for (uint32_t k = 0;; ++k) {
+        const int s = int(k % STAGES);
+        const uint32_t par = (k / STAGES) & 1u;
+        const int w = warp_wait_or_end(sm.full(s), par, k, sm.end_iter());
+        if (w != 2 || !warp_wait(sm.carry_ready(s), par)) {
+            if (w != 1 && lane == 0) record_error(hdr, DWP_ERR_PIPELINE_TIMEOUT);
+            break;
+        }
+        const uint32_t t = ld_volatile_smem(sm.tile_id(s));
+        if (t == kNoTile) break;
+        uint32_t valid, bulk;
+        tile_extent(t, valid, bulk);
+        const uint64_t base = uint64_t(t) * TILE;
+        // a tile wholly inside [cover_lo, cover_hi) is stored in bulk; any
+        // other tile row by row, only the covered rows
+        const bool covered = base >= cover_lo && base + valid <= cover_hi;
+        if (ld_volatile_smem(sm.lbres(s)) != 0u || (!covered && (base >= cover_hi || base + valid <= cover_lo))) {
+            if (lane == 0) {
+                bulk_wait_read<0>();
+                if (pending >= 0) mbar_arrive(sm.empty(pending));
+                mbar_arrive(sm.empty(s));
+                pending = -1;
+            }
+            __syncwarp();
+            continue;
+        }
+        uint32_t *buf = sm.data(s);
+        const uint32_t p0 = c * ITEMS;
+        const uint32_t hb = head_bits(sm.heads(s), p0, ITEMS);
+        const bool ph = sm.phead(s)[c] != 0;
+        const uint32_t pv = sm.prefix(s)[prefix_slot(c)];
+        uint32_t acc = ph ? pv : *sm.carry(s) + pv;
+        if (valid == uint32_t(TILE) && covered) {
+            uint4 *v4 = reinterpret_cast<uint4 *>(buf + p0);
+#pragma unroll
+            for (int v = 0; v < ITEMS / 4; ++v) {
+                const uint4 q = v4[v];
+                const uint32_t qq[4] = {q.x, q.y, q.z, q.w};
+                uint32_t r[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if ((hb >> (4 * v + e)) & 1u) acc = 0u;
+                    if (INCL) {
+                        acc += qq[e];
+                        r[e] = acc;
+                    } else {
+                        r[e] = acc;
+                        acc += qq[e];
+                    }
+                }
+                v4[v] = make_uint4(r[0], r[1], r[2], r[3]);
+            }
+        } else {
+            for (int j = 0; j < ITEMS; ++j) {
+                const uint32_t pos = p0 + j;
+                const uint32_t x = seg_elem(buf, in, base, pos, bulk, valid);
+                if ((hb >> j) & 1u) acc = 0u;
+                uint32_t y;
+                if (INCL) {
+                    acc += x;
+                    y = acc;
+                } else {
+                    y = acc;
+                    acc += x;
+                }
+                const uint64_t g = base + pos;
+                if (pos < valid && covered && pos < bulk)
+                    buf[pos] = y;
+                else if (pos < valid && g >= cover_lo && g < cover_hi)
+                    out[g] = y;
+            }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            const uint32_t w0 = cw * WE;
+            const uint32_t w1 = covered ? min(w0 + uint32_t(WE), bulk) : w0;
+            if (w1 > w0) {
+                bulk_store(out + base + w0, buf + w0, (w1 - w0) * 4u);
+                bulk_commit();
+                bulk_wait_read<1>();
+                if (pending >= 0) mbar_arrive(sm.empty(pending));
+                pending = s;
+            } else {
+                bulk_wait_read<0>();
+                if (pending >= 0) mbar_arrive(sm.empty(pending));
+                mbar_arrive(sm.empty(s));
+                pending = -1;
+            }
+        }
+        __syncwarp();
+    }
+    if (lane == 0) bulk_wait_all<0>();
+}
+
+template <bool INCL>
+cudaError_t launch_seg(const uint32_t *values, const uint32_t *offsets, uint32_t nseg,
+                       uint32_t *out, uint64_t n, void *scratch, cudaStream_t stream,
+                       const FaultConfig &fault) {
+    using C = SegCfg;
+    auto kern = segscan_kernel<INCL, C>;
+    const int dev_blocks = device_blocks(reinterpret_cast<const void *>(kern), C::kThreads,
+                                         C::kSmemBytes);
+    if (dev_blocks <= 0) return cudaErrorInvalidConfiguration;
+    const uint64_t tiles = (n + C::kTile - 1) / C::kTile;
+    const uint32_t grid = uint32_t(tiles < uint64_t(dev_blocks) ? tiles : uint64_t(dev_blocks));
+    auto *hdr = reinterpret_cast<ScratchHeader *>(scratch);
+    auto *desc = reinterpret_cast<uint64_t *>(static_cast<unsigned char *>(scratch) + kHeaderBytes);
+    kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(values, offsets, nseg, out, n,
+                                                       uint32_t(tiles), hdr, desc, fault);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+uint32_t segscan_tile_elems() { return SegCfg::kTile; }
+
+cudaError_t launch_segscan(const uint32_t *values, const uint32_t *offsets, uint32_t nseg,
+                           uint32_t *out, uint64_t n, bool inclusive, void *scratch,
+                           cudaStream_t stream) {
+    const FaultConfig fault = current_fault_config();
+    return inclusive ? launch_seg<true>(values, offsets, nseg, out, n, scratch, stream, fault)
+                     : launch_seg<false>(values, offsets, nseg, out, n, scratch, stream, fault);
+}
+
+}  // namespace dwp

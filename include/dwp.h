@@ -104,6 +104,36 @@ dwp_status dwp_scan_inclusive(dwp_op op, const void *d_in, void *d_out, size_t n
                               void *d_scratch, size_t *scratch_bytes, dwp_stream stream);
 
 /*
+ * Segmented uint32 addition scan over CSR offsets ("GPUSegmentedScan",
+ * sections "Prefix scans and segmented scans", "Contract" and
+ * "Limitations"; "Parallel Prefix Sum (Scan), in depth", section "What scan
+ * builds": the running total restarts at every segment boundary).
+ *   d_values      device uint32[n], 16-byte aligned
+ *   d_offsets     device uint32[num_segments + 1], 4-byte aligned; segment
+ *                 s is rows [d_offsets[s], d_offsets[s+1]).  Offsets are
+ *                 trusted: non-decreasing with d_offsets[num_segments] <= n
+ *                 is a precondition the device does not check (no
+ *                 readback); broken offsets give unspecified values but no
+ *                 access out of range.  Repeated offsets are empty
+ *                 segments and write no rows.
+ *   num_segments  N, 0 <= N < 2^32 - 1 (N + 1 offsets are read).
+ *   d_out         device uint32[n], 16-byte aligned.  Rows outside
+ *                 [d_offsets[0], min(d_offsets[N], n)) are left unwritten.
+ *                 Overlap with d_values, d_offsets or d_scratch is
+ *                 DWP_ERR_ALIASING.
+ *   n             row count, 0 <= n < 2^32.
+ *   mode          DWP_EXCLUSIVE (a segment's first row is 0) or
+ *                 DWP_INCLUSIVE.
+ *   d_scratch, scratch_bytes, stream: as dwp_scan_exclusive (the size
+ *                 query depends on n only).
+ * u32 sums wrap modulo 2^32.  Results are bit-exact and deterministic.
+ */
+dwp_status dwp_segmented_scan_u32(const uint32_t *d_values, const uint32_t *d_offsets,
+                                  size_t num_segments, uint32_t *d_out, size_t n,
+                                  dwp_mode mode, void *d_scratch, size_t *scratch_bytes,
+                                  dwp_stream stream);
+
+/*
  * Scan for callers that cannot allocate device memory.  The source pages
  * have no counterpart to this entry point; it is a convenience of this
  * library.  Code that runs inside another framework's allocator hooks or

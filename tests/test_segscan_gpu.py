@@ -1,0 +1,138 @@
+"""Parity of the CUDA segmented u32 scan (through the C ABI) with the oracle:
+bit-exact on every row, rows outside [offsets[0], offsets[N]) untouched."""
+import numpy as np
+import pytest
+
+import golden_io
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import device_wide_prefix_gb300 as dwp  # noqa: E402
+from device_wide_prefix_gb300 import build as dwp_build  # noqa: E402
+
+SENTINEL = 0xDEADBEEF
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    dwp_build.build()
+    return dwp.load()
+
+
+@pytest.fixture(scope="module")
+def ref():
+    return oracle.Oracle()
+
+
+def tile():
+    b1 = dwp.segmented_scan_scratch_bytes(1)
+    T = 1
+    while dwp.segmented_scan_scratch_bytes(2 * T) == b1:
+        T *= 2
+    lo, hi = T, 2 * T
+    while hi - lo > 1:
+        mid = (lo + hi) // 2
+        if dwp.segmented_scan_scratch_bytes(mid) == b1:
+            lo = mid
+        else:
+            hi = mid
+    return lo
+
+
+def gpu_seg(values, offsets, inclusive):
+    v = torch.from_numpy(values.view(np.int32)).cuda()
+    o = torch.from_numpy(np.ascontiguousarray(offsets, dtype=np.uint32).view(np.int32)).cuda()
+    out = torch.full((values.size,), SENTINEL - (1 << 32), dtype=torch.int32, device="cuda")
+    scratch = dwp.alloc_scratch(dwp.segmented_scan_scratch_bytes(values.size), v.device)
+    dwp.segmented_scan(v, o, inclusive, out=out, scratch=scratch)
+    assert dwp.read_status(scratch) == dwp.DWP_SUCCESS
+    return out.cpu().numpy().view(np.uint32)
+
+
+def check(ref, values, offsets, inclusive):
+    want = ref.segmented_scan_u32(values, offsets, inclusive,
+                                  out=np.full(values.size, SENTINEL, np.uint32))
+    got = gpu_seg(values, offsets, inclusive)
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, "mismatch at %s: got %s want %s" % (bad[:5], got[bad[:5]], want[bad[:5]])
+
+
+def test_golden_example():
+    ex = golden_io.load()["segmented_luma"]
+    v = np.array(ex["values"], np.uint32)
+    off = np.array(ex["offsets"], np.uint32)
+    assert gpu_seg(v, off, False).tolist() == ex["exclusive"]
+    assert gpu_seg(v, off, True).tolist() == ex["inclusive"]
+
+
+@pytest.mark.parametrize("inclusive", [False, True], ids=["excl", "incl"])
+def test_segment_shapes(ref, inclusive):
+    T = tile()
+    n = 5 * T + 77
+    v = synth.u32_full_values(n, 501)
+    shapes = {
+        "one_segment": [0, n],
+        "all_length_one": list(range(n + 1)),
+        "leading_trailing_consecutive_empties": [0, 0, 0, 5, 5, 100, 100, 100, T, 2 * T - 1, n, n, n],
+        "partial_cover": [7, 7, 40, T + 3, 3 * T + 11],
+        "heads_on_tile_edges": [0, T, 2 * T, 3 * T, 4 * T, 5 * T, n],
+        "heads_next_to_tile_edges": [0, T - 1, T + 1, 2 * T - 1, 3 * T + 1, n],
+        "many_empties_at_one_row": [0] + [T + 5] * 3000 + [n],
+        "one_segment_many_tiles_then_short": [0, 4 * T + 9, 4 * T + 10, n],
+        "first_row_not_covered": [1, n],
+        "last_row_not_covered": [0, n - 1],
+    }
+    for name, offs in shapes.items():
+        check(ref, v, np.array(offs, np.uint32), inclusive)
+
+
+@pytest.mark.parametrize("inclusive", [False, True], ids=["excl", "incl"])
+def test_many_segments_global_search(ref, inclusive):
+    """More offsets than the per-block sample holds: the head search falls back
+    to the warp-wide search in global memory."""
+    n = 1 << 20
+    v = synth.u32_byte_values(n, 502)
+    u = synth.u64(503, 0, n)
+    lens = (u % np.uint64(100)).astype(np.int64)  # 0 .. 99, with empties
+    cum = np.cumsum(lens)
+    cum = cum[cum < n]
+    off = np.concatenate([[0], cum, [n]]).astype(np.uint32)
+    assert off.size > 5000
+    check(ref, v, off, inclusive)
+    check(ref, v[: 300001].copy(), np.arange(300002, dtype=np.uint32), inclusive)
+
+
+@pytest.mark.parametrize("inclusive", [False, True], ids=["excl", "incl"])
+def test_zipf_lengths_small(ref, inclusive):
+    n = 1 << 21
+    off = synth.segment_offsets(n, seed=504, cap=1 << 16)
+    check(ref, synth.u32_byte_values(n, 505), off, inclusive)
+
+
+def test_degenerate_sizes(ref):
+    T = tile()
+    for n in (1, 2, 3, 4, 5, 31, 33, T - 1, T, T + 1):
+        v = synth.u32_full_values(n, 506)
+        for offs in ([0, n], [0, n // 2, n], [0] * 3 + [n]):
+            for inc in (False, True):
+                check(ref, v, np.array(offs, np.uint32), inc)
+    # no segments: nothing is written
+    v = synth.u32_full_values(1000, 507)
+    assert (gpu_seg(v, np.array([0], np.uint32), False) == SENTINEL).all()
+    # no rows
+    assert gpu_seg(np.zeros(0, np.uint32), np.array([0, 0], np.uint32), True).size == 0
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("inclusive", [False, True], ids=["excl", "incl"])
+def test_full_skewed_2p27(ref, inclusive):
+    """n = 2^27 values in [0, 255]; Zipf(1.2) lengths capped at 2^22, 5% empty."""
+    n = 1 << 27
+    off = synth.segment_offsets(n)
+    check(ref, synth.u32_byte_values(n), off, inclusive)
