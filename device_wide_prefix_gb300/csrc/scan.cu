@@ -100,35 +100,6 @@ struct ScanSmem {
     __device__ uint32_t *end_iter() const { return abort_flag() + 1; }
 };
 
-// Word index of consumer thread c's prefix: one pad word after every 8.
-__device__ __forceinline__ uint32_t prefix_slot(uint32_t c) { return c + (c >> 3); }
-
-// Bounded mbarrier wait agreed by the whole warp (every lane polls).
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity) {
-    return __all_sync(0xffffffffu, mbar_wait(bar, parity, kPipeWaitLimit));
-}
-
-// Wait for ring iteration k's data, or learn that the producer stopped
-// before iteration k (end_iter < k).  Warp-uniform result: 2 data ready,
-// 1 ended, 0 poll limit reached.  Ready and ended cannot both hold for one k:
-// the producer fills only iterations up to end_iter.
-__device__ __forceinline__ int warp_wait_or_end(uint64_t *bar, uint32_t parity, uint32_t k,
-                                                const uint32_t *end_iter) {
-    uint32_t r = 0;
-    for (uint32_t i = 0; i < kPipeWaitLimit; ++i) {
-        if (mbar_try_wait(bar, parity)) {
-            r = 2;
-            break;
-        }
-        if (ld_volatile_smem(end_iter) < k) {
-            r = 1;
-            break;
-        }
-        if (i >= 8) __nanosleep(64);
-    }
-    return int(__reduce_max_sync(0xffffffffu, r));
-}
-
 // Element pos of a tile: from the stage buffer below `bulk`, from global
 // memory below `valid` (the ragged tail the bulk copy cannot cover), else the
 // identity.

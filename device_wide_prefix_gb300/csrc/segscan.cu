@@ -107,29 +107,6 @@ struct SegSmem {
     __device__ uint32_t *sample() const { return words() + 4; }
 };
 
-__device__ __forceinline__ uint32_t prefix_slot(uint32_t c) { return c + (c >> 3); }
-
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity) {
-    return __all_sync(0xffffffffu, mbar_wait(bar, parity, kPipeWaitLimit));
-}
-
-__device__ __forceinline__ int warp_wait_or_end(uint64_t *bar, uint32_t parity, uint32_t k,
-                                                const uint32_t *end_iter) {
-    uint32_t r = 0;
-    for (uint32_t i = 0; i < kPipeWaitLimit; ++i) {
-        if (mbar_try_wait(bar, parity)) {
-            r = 2;
-            break;
-        }
-        if (ld_volatile_smem(end_iter) < k) {
-            r = 1;
-            break;
-        }
-        if (i >= 8) __nanosleep(64);
-    }
-    return int(__reduce_max_sync(0xffffffffu, r));
-}
-
 __device__ __forceinline__ uint32_t seg_elem(const uint32_t *buf, const uint32_t *in, uint64_t base,
                                              uint32_t pos, uint32_t bulk, uint32_t valid) {
     if (pos < bulk) return buf[pos];
