@@ -43,6 +43,7 @@ EXPORTS = [
     "dwp_scan_exclusive",
     "dwp_scan_inclusive",
     "dwp_segmented_scan_u32",
+    "dwp_compact_by_flags",
     "dwp_read_status",
     "dwp_status_string",
     "dwp_version",
@@ -77,6 +78,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         f.restype = c.c_int
     lib.dwp_segmented_scan_u32.argtypes = [P, P, S, P, S, c.c_int, P, Z, P]
     lib.dwp_segmented_scan_u32.restype = c.c_int
+    lib.dwp_compact_by_flags.argtypes = [P, P, S, P, P, P, Z, P]
+    lib.dwp_compact_by_flags.restype = c.c_int
     lib.dwp_read_status.argtypes = [P, P]
     lib.dwp_read_status.restype = c.c_int
     lib.dwp_status_string.argtypes = [c.c_int]
@@ -120,6 +123,15 @@ def dwp_segmented_scan_u32(d_values, d_offsets, num_segments, d_out, n, mode, d_
     st = load().dwp_segmented_scan_u32(d_values or None, d_offsets or None, num_segments,
                                        d_out or None, n, int(mode), d_scratch or None,
                                        ctypes.byref(sb), stream or None)
+    return st, sb.value
+
+
+def dwp_compact_by_flags(d_records, d_flags, n, d_out, d_count, d_scratch, scratch_bytes, stream):
+    """dwp.h dwp_compact_by_flags; returns (status, scratch_bytes after the call)."""
+    sb = ctypes.c_size_t(scratch_bytes)
+    st = load().dwp_compact_by_flags(d_records or None, d_flags or None, n, d_out or None,
+                                     d_count or None, d_scratch or None, ctypes.byref(sb),
+                                     stream or None)
     return st, sb.value
 
 
@@ -251,6 +263,38 @@ def segmented_scan(values, offsets, inclusive: bool = False, out=None, scratch=N
                                        scratch.data_ptr(), scratch.numel(), _stream_of(values, stream))
     _check(st, "dwp_segmented_scan_u32")
     return out
+
+
+def compact_scratch_bytes(n: int) -> int:
+    st, b = dwp_compact_by_flags(None, None, n, None, None, None, 0, None)
+    _check(st, "compaction scratch size query")
+    return b
+
+
+def compact_by_flags(records, flags, out=None, count=None, scratch=None, stream=None):
+    """Stable compaction of `records` (CUDA tensor, 16 bytes per row, e.g.
+    shape (n, 4) int32) by `flags` (CUDA uint8, n).  Returns (out, count) with
+    count a 1-element CUDA int32 tensor; rows of `out` past the count are
+    untouched."""
+    torch = _torch()
+    n = flags.numel()
+    if not (records.is_cuda and flags.is_cuda and records.is_contiguous() and flags.is_contiguous()):
+        raise ValueError("records and flags must be contiguous CUDA tensors")
+    if records.numel() * records.element_size() != 16 * n or flags.element_size() != 1:
+        raise ValueError("records must hold 16 bytes per flag byte")
+    if out is None:
+        out = torch.empty_like(records)
+    if count is None:
+        count = torch.empty(1, dtype=torch.int32, device=records.device)
+    need = compact_scratch_bytes(n)
+    if scratch is None:
+        scratch = alloc_scratch(need, records.device)
+    with torch.cuda.device(records.device):
+        st, _ = dwp_compact_by_flags(records.data_ptr(), flags.data_ptr(), n, out.data_ptr(),
+                                     count.data_ptr(), scratch.data_ptr(), scratch.numel(),
+                                     _stream_of(records, stream))
+    _check(st, "dwp_compact_by_flags")
+    return out, count
 
 
 def read_status(scratch, stream=None) -> int:

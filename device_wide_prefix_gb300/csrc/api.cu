@@ -99,9 +99,58 @@ dwp_status segscan_common(const uint32_t *values, const uint32_t *offsets, size_
     return DWP_SUCCESS;
 }
 
+dwp_status compact_common(const void *records, const uint8_t *flags, size_t n, void *out,
+                          uint32_t *count, void *scratch, size_t *scratch_bytes,
+                          dwp_stream stream) {
+    if (!scratch_bytes) return DWP_ERR_INVALID_VALUE;
+    if (uint64_t(n) > kMaxN) return DWP_ERR_INVALID_VALUE;
+    const uint64_t tiles = ceil_div(n, compact_tile_records());
+    const size_t need = scratch_bytes_for_tiles(tiles);
+    if (!scratch) {
+        *scratch_bytes = need;
+        return DWP_SUCCESS;
+    }
+    if (*scratch_bytes < need) return DWP_ERR_SCRATCH_TOO_SMALL;
+    if (!count || (n > 0 && (!records || !flags || !out))) return DWP_ERR_INVALID_VALUE;
+    if (!aligned16(scratch) || !aligned4(count) ||
+        (n > 0 && (!aligned16(records) || !aligned16(flags) || !aligned16(out))))
+        return DWP_ERR_MISALIGNED;
+    const uint64_t rbytes = uint64_t(n) * 16u, fbytes = uint64_t(n);
+    if (overlap(out, rbytes, records, rbytes) || overlap(out, rbytes, flags, fbytes) ||
+        overlap(out, rbytes, count, 4) || overlap(out, rbytes, scratch, need) ||
+        overlap(count, 4, records, rbytes) || overlap(count, 4, flags, fbytes) ||
+        overlap(count, 4, scratch, need) || overlap(scratch, need, records, rbytes) ||
+        overlap(scratch, need, flags, fbytes))
+        return DWP_ERR_ALIASING;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(scratch, 0, need, s) != cudaSuccess) {
+        cudaGetLastError();
+        return DWP_ERR_CUDA;
+    }
+    if (n == 0) {
+        if (cudaMemsetAsync(count, 0, sizeof(uint32_t), s) != cudaSuccess) {
+            cudaGetLastError();
+            return DWP_ERR_CUDA;
+        }
+        return DWP_SUCCESS;
+    }
+    if (launch_compact(records, flags, n, out, count, scratch, s) != cudaSuccess) {
+        cudaGetLastError();
+        return DWP_ERR_CUDA;
+    }
+    return DWP_SUCCESS;
+}
+
 }  // namespace
 
 extern "C" {
+
+dwp_status dwp_compact_by_flags(const void *d_records, const uint8_t *d_flags, size_t n,
+                                void *d_out, uint32_t *d_count, void *d_scratch,
+                                size_t *scratch_bytes, dwp_stream stream) {
+    return compact_common(d_records, d_flags, n, d_out, d_count, d_scratch, scratch_bytes, stream);
+}
 
 dwp_status dwp_segmented_scan_u32(const uint32_t *d_values, const uint32_t *d_offsets,
                                   size_t num_segments, uint32_t *d_out, size_t n, dwp_mode mode,

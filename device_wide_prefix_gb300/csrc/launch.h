@@ -26,4 +26,10 @@ cudaError_t launch_segscan(const uint32_t *values, const uint32_t *offsets, uint
                            uint32_t *out, uint64_t n, bool inclusive, void *scratch,
                            cudaStream_t stream);
 
+// Records per tile of the compaction kernel.
+uint32_t compact_tile_records();
+// One launch of the stable compaction (scratch already cleared; n >= 1).
+cudaError_t launch_compact(const void *records, const uint8_t *flags, uint64_t n, void *out,
+                           uint32_t *count, void *scratch, cudaStream_t stream);
+
 }  // namespace dwp

@@ -134,6 +134,30 @@ dwp_status dwp_segmented_scan_u32(const uint32_t *d_values, const uint32_t *d_of
                                   dwp_stream stream);
 
 /*
+ * Stable stream compaction of 16-byte records by byte flags ("Prefix scans
+ * and compaction", sections "Scan as an index generator" and "Worked
+ * example: Stable stream compaction"; "Parallel Prefix Sum (Scan), in
+ * depth", section "What scan builds").  Record i is kept when d_flags[i] is
+ * nonzero and is written to slot (number of kept records before i) of
+ * d_out, so kept records keep their input order; the number kept goes to
+ * *d_count.
+ *   d_records     device array of n records of 16 bytes each (opaque,
+ *                 copied bit for bit), 16-byte aligned
+ *   d_flags       device uint8[n], 16-byte aligned
+ *   n             record count, 0 <= n < 2^32
+ *   d_out         device array with room for n records, 16-byte aligned;
+ *                 slots at and past the kept count are left unwritten.
+ *   d_count       device uint32, 4-byte aligned: receives the kept count
+ *                 (0 for n == 0).
+ *   d_scratch, scratch_bytes, stream: as dwp_scan_exclusive.
+ * Any overlap among d_out, d_count, d_scratch and the inputs is
+ * DWP_ERR_ALIASING.  Results are bit-exact and deterministic.
+ */
+dwp_status dwp_compact_by_flags(const void *d_records, const uint8_t *d_flags, size_t n,
+                                void *d_out, uint32_t *d_count, void *d_scratch,
+                                size_t *scratch_bytes, dwp_stream stream);
+
+/*
  * Scan for callers that cannot allocate device memory.  The source pages
  * have no counterpart to this entry point; it is a convenience of this
  * library.  Code that runs inside another framework's allocator hooks or
