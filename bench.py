@@ -400,7 +400,37 @@ def measure_secondary(dwp, lib, dev, stream, peaks, x, y, scratch, need) -> dict
                      "frac": gbs / peaks["hbm_gbs"]}
     del xf
     out["segscan_u32_exclusive"] = measure_segscan(dwp, lib, dev, stream, peaks)
+    out["compact_16B_records"] = measure_compact(dwp, lib, dev, stream, peaks)
     return out
+
+
+def measure_compact(dwp, lib, dev, stream, peaks) -> dict:
+    """Stable compaction of 2^26 16-byte records {u32 id, 3 x f32 N(0,1)} by
+    Bernoulli(0.3) byte flags."""
+    import ctypes
+    import torch
+    n = 1 << 26
+    rec = torch.from_numpy(synth.records(n).view(np.int32)).to(dev)
+    flags = torch.from_numpy(synth.keep_flags(n)).to(dev)
+    out = torch.empty_like(rec)
+    cnt = torch.zeros(1, dtype=torch.int32, device=dev)
+    need = dwp.compact_scratch_bytes(n)
+    scratch = dwp.alloc_scratch(need, dev)
+    sb = ctypes.c_size_t(need)
+    args = (ctypes.c_void_p(rec.data_ptr()), ctypes.c_void_p(flags.data_ptr()), n,
+            ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(cnt.data_ptr()),
+            ctypes.c_void_p(scratch.data_ptr()), ctypes.byref(sb),
+            ctypes.c_void_p(int(stream.cuda_stream)))
+    ms = time_calls(lambda: lib.dwp_compact_by_flags(*args), 100, 5, stream)
+    if dwp.read_status(scratch) != dwp.DWP_SUCCESS:
+        raise RuntimeError("compaction reported a device-side error")
+    k = int(cnt.item())
+    alg = 17 * n + 16 * k + 4
+    gbs = alg / (ms * 1e-3) / 1e9
+    return {"n": n, "kept": k, "ms": ms, "Gelem_s": n / (ms * 1e-3) / 1e9, "GB_s": gbs,
+            "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": alg,
+            "workload": "stable compaction of 2^26 16-byte records, keep flag Bernoulli(0.3) "
+                        "(SplitMix64 seed 0xD3B00004)"}
 
 
 def measure_segscan(dwp, lib, dev, stream, peaks) -> dict:
