@@ -127,6 +127,36 @@ __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gmem_src, 
         : "memory");
 }
 
+// L2 eviction-priority policies for bulk copies (createpolicy, sm_80+).
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// bulk_load with an L2 eviction-priority policy for the lines it reads.
+__device__ __forceinline__ void bulk_load_hint(void *smem_dst, const void *gmem_src, uint32_t bytes,
+                                               uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(smem_dst)),
+        "l"(gmem_src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+// bulk_store with an L2 eviction-priority policy for the lines it writes.
+__device__ __forceinline__ void bulk_store_hint(void *gmem_dst, const void *smem_src, uint32_t bytes,
+                                                uint64_t policy) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(gmem_dst),
+                 "r"(smem_addr(smem_src)), "r"(bytes), "l"(policy)
+                 : "memory");
+}
+
 // Bulk shared -> global copy in the current bulk async-group.
 __device__ __forceinline__ void bulk_store(void *gmem_dst, const void *smem_src, uint32_t bytes) {
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gmem_dst),

@@ -3,22 +3,37 @@
 // One persistent, warp-specialised launch ("Single-Pass Prefix Scan with
 // Decoupled Look-Back"; "Parallel Prefix Sum (Scan), in depth", sections "A
 // CUDA scan: warp, block, grid" and "Scanning a whole array: three grid
-// strategies").  A block owns a ring of STAGES tile buffers in shared memory:
+// strategies").  Per block:
 //
-//   producer warp   takes tile indices from the atomic counter in the order
-//                   tiles start and streams each tile global -> shared with
-//                   one bulk (TMA) copy;
-//   tile warps      one per stage.  For its tile: every consumer thread's
-//                   total and their exclusive prefix (block layer), the
-//                   aggregate published as soon as the data has landed, the
-//                   look-back, the inclusive prefix published, the carry
-//                   handed over.  With one warp per stage a block has up to
-//                   STAGES look-backs in flight, so a slow predecessor
-//                   delays only the tiles that need it;
-//   consumer warps  warp w owns chunk w of every tile; each thread scans its
-//                   ITEMS contiguous elements serially from carry + its
-//                   in-tile prefix, writes them back in place, and the warp
-//                   streams its chunk shared -> global with one bulk store.
+//   producer warp    takes tile indices from the atomic counter in the order
+//                    tiles start and streams each tile global -> shared with
+//                    one bulk (TMA) copy into a ring of SIN input stages;
+//   reducer warps    one per input stage.  For its tile: every consumer
+//                    thread's total and their exclusive prefix (block
+//                    layer), written to a slot of the tile-info ring; the
+//                    aggregate published at once; the input stage freed;
+//   look-back warps  LW of them, iteration k taken by warp k % LW: the
+//                    look-back, the inclusive prefix published, the carry
+//                    written to the tile's info slot;
+//   reloader warp    once a tile's carry is known, brings the tile back with
+//                    one bulk copy into a ring of SOUT output stages.  The
+//                    tile was read from HBM some microseconds earlier and
+//                    still sits in the L2 (129 MB), so this copy costs L2
+//                    bandwidth, not HBM bandwidth.  For that the first load
+//                    marks the tile's lines evict-last, the reload and the
+//                    output stores evict-first (without the hints about 60%
+//                    of the reloads missed L2 and went back to HBM);
+//   consumer warps   warp w owns chunk w of every tile; each thread scans its
+//                    ITEMS contiguous elements serially from carry + its
+//                    in-tile prefix, writes them back in place, and the warp
+//                    streams its chunk shared -> global with one bulk store.
+//
+// Why the reload: a tile cannot finish before every earlier tile has
+// published its aggregate, and tiles land from HBM out of order by several
+// microseconds, so the look-back of a tile waits a few microseconds.  Held
+// in shared memory for that wait, the tiles in flight per SM exceeded shared
+// memory at full bandwidth; held in L2 they do not.  Shared memory now holds
+// a tile only while it is reduced and while it is scanned and stored.
 //
 // ITEMS is an odd multiple of 4, so the 16-byte shared-memory accesses of a
 // quarter warp (thread stride 16*odd bytes) fall in 8 distinct bank groups.
@@ -31,70 +46,94 @@
 
 namespace dwp {
 
-template <int NW_, int ITEMS_, int STAGES_, int LOOKK_, int MINB_>
+template <int NW_, int ITEMS_, int SIN_, int SOUT_, int RING_, int LW_, int LOOKK_>
 struct ScanConfig {
-    static constexpr int kWarps = NW_;        // consumer warps (one chunk of the tile each)
-    static constexpr int kItems = ITEMS_;     // contiguous elements per consumer thread
-    static constexpr int kStages = STAGES_;   // shared-memory ring depth = tile warps
-    static constexpr int kLookK = LOOKK_;     // look-back sub-windows of 32 per round
-    static constexpr int kMinBlocks = MINB_;  // resident blocks per SM the registers allow
-    static constexpr int kThreads = (1 + STAGES_ + NW_) * 32;
+    static constexpr int kWarps = NW_;       // consumer warps (one chunk of the tile each)
+    static constexpr int kItems = ITEMS_;    // contiguous elements per consumer thread
+    static constexpr int kIn = SIN_;         // input stages = reducer warps
+    static constexpr int kOut = SOUT_;       // output stages
+    static constexpr int kRing = RING_;      // tile-info slots
+    static constexpr int kLookers = LW_;     // look-back warps
+    static constexpr int kLookK = LOOKK_;    // look-back sub-windows of 32 per poll
+    static constexpr int kThreads = (2 + SIN_ + LW_ + NW_) * 32;
     static constexpr int kConsumers = NW_ * 32;
     static constexpr int kWarpElems = 32 * ITEMS_;
     static constexpr int kTile = NW_ * 32 * ITEMS_;
     static_assert(ITEMS_ % 4 == 0 && (ITEMS_ / 4) % 2 == 1, "ITEMS must be an odd multiple of 4");
     static_assert(NW_ >= 1 && NW_ <= 32, "one 32-slot row of thread totals per consumer warp");
+    static_assert(RING_ % LW_ == 0, "a look-back warp must own every use of its info slots");
+    static_assert(SOUT_ >= 2, "the reloader waits for the output stage of iteration k - SOUT");
+    static_assert(RING_ >= SIN_ + SOUT_ + 2, "info ring shorter than the work in flight");
     static constexpr size_t kStageBytes = size_t(kTile) * 4;
-    // Per stage after the data: 3 mbarriers (+pad, 32 B); tile id, aggregate,
-    // carry, look-back result (16 B); thread prefixes, one word per consumer
-    // thread plus one pad word per 8 (bank spread); 33 lane totals; 33 words
-    // of look-back scratch.
     static constexpr int kPrefixWords = kConsumers + kConsumers / 8;
-    static constexpr size_t kStageMeta = 48 + 4 * (kPrefixWords + 33 + 33);
-    // + abort flag and end iteration
-    static constexpr size_t kSmemBytes = (kStageBytes + kStageMeta) * kStages + 16;
+    // info slot: 3 mbarriers + pad (32 B); tile id, aggregate, carry,
+    // look-back result (16 B); thread prefixes; 33 lane totals; 33 words of
+    // look-back scratch
+    static constexpr size_t kInfoBytes = 48 + 4 * (kPrefixWords + 33 + 33);
+    // stage barriers: per input stage full + empty, per output stage ready + empty
+    static constexpr size_t kBarBytes = 16 * (SIN_ + SOUT_);
+    static constexpr size_t kSmemBytes =
+        kStageBytes * (SIN_ + SOUT_) + kInfoBytes * RING_ + kBarBytes + 16;
 };
 
 #ifndef DWP_SCAN_WARPS
-#define DWP_SCAN_WARPS 16
+#define DWP_SCAN_WARPS 8
 #endif
 #ifndef DWP_SCAN_ITEMS
 #define DWP_SCAN_ITEMS 20
 #endif
-#ifndef DWP_SCAN_STAGES
-#define DWP_SCAN_STAGES 5
+#ifndef DWP_SCAN_IN
+#define DWP_SCAN_IN 5
+#endif
+#ifndef DWP_SCAN_OUT
+#define DWP_SCAN_OUT 4
+#endif
+#ifndef DWP_SCAN_RING
+#define DWP_SCAN_RING 16
+#endif
+#ifndef DWP_SCAN_LOOKERS
+#define DWP_SCAN_LOOKERS 8
 #endif
 #ifndef DWP_SCAN_LOOKK
 #define DWP_SCAN_LOOKK 4
 #endif
-#ifndef DWP_SCAN_MINB
-#define DWP_SCAN_MINB 1
-#endif
-using ScanCfg = ScanConfig<DWP_SCAN_WARPS, DWP_SCAN_ITEMS, DWP_SCAN_STAGES, DWP_SCAN_LOOKK,
-                           DWP_SCAN_MINB>;
+using ScanCfg = ScanConfig<DWP_SCAN_WARPS, DWP_SCAN_ITEMS, DWP_SCAN_IN, DWP_SCAN_OUT,
+                           DWP_SCAN_RING, DWP_SCAN_LOOKERS, DWP_SCAN_LOOKK>;
 
 // Shared-memory layout of one block.
 template <class C>
 struct ScanSmem {
     unsigned char *base;
     __device__ explicit ScanSmem(unsigned char *p) : base(p) {}
-    __device__ uint32_t *data(int s) const {
+    __device__ uint32_t *in_data(int s) const {
         return reinterpret_cast<uint32_t *>(base + size_t(s) * C::kStageBytes);
     }
-    __device__ unsigned char *meta(int s) const {
-        return base + C::kStageBytes * C::kStages + size_t(s) * C::kStageMeta;
+    __device__ uint32_t *out_data(int o) const {
+        return reinterpret_cast<uint32_t *>(base + size_t(C::kIn + o) * C::kStageBytes);
     }
-    __device__ uint64_t *full(int s) const { return reinterpret_cast<uint64_t *>(meta(s)); }
-    __device__ uint64_t *carry_ready(int s) const { return full(s) + 1; }
-    __device__ uint64_t *empty(int s) const { return full(s) + 2; }
-    __device__ uint32_t *tile_id(int s) const { return reinterpret_cast<uint32_t *>(meta(s) + 32); }
-    __device__ uint32_t *carry(int s) const { return tile_id(s) + 1; }
-    __device__ uint32_t *lbres(int s) const { return tile_id(s) + 2; }
-    __device__ uint32_t *prefix(int s) const { return tile_id(s) + 4; }
-    __device__ uint32_t *lane_tot(int s) const { return prefix(s) + C::kPrefixWords; }
-    __device__ uint32_t *lb_scratch(int s) const { return lane_tot(s) + 33; }
+    __device__ unsigned char *info(int i) const {
+        return base + C::kStageBytes * (C::kIn + C::kOut) + size_t(i) * C::kInfoBytes;
+    }
+    __device__ uint64_t *info_ready(int i) const { return reinterpret_cast<uint64_t *>(info(i)); }
+    __device__ uint64_t *carry_ready(int i) const { return info_ready(i) + 1; }
+    __device__ uint64_t *info_free(int i) const { return info_ready(i) + 2; }
+    __device__ uint32_t *tile_id(int i) const { return reinterpret_cast<uint32_t *>(info(i) + 32); }
+    __device__ uint32_t *agg(int i) const { return tile_id(i) + 1; }
+    __device__ uint32_t *carry(int i) const { return tile_id(i) + 2; }
+    __device__ uint32_t *lbres(int i) const { return tile_id(i) + 3; }
+    __device__ uint32_t *prefix(int i) const { return tile_id(i) + 4; }
+    __device__ uint32_t *lane_tot(int i) const { return prefix(i) + C::kPrefixWords; }
+    __device__ uint32_t *lb_scratch(int i) const { return lane_tot(i) + 33; }
+    __device__ uint64_t *bars() const {
+        return reinterpret_cast<uint64_t *>(base + C::kStageBytes * (C::kIn + C::kOut) +
+                                            C::kInfoBytes * C::kRing);
+    }
+    __device__ uint64_t *in_full(int s) const { return bars() + s; }
+    __device__ uint64_t *in_empty(int s) const { return bars() + C::kIn + s; }
+    __device__ uint64_t *out_full(int o) const { return bars() + 2 * C::kIn + o; }
+    __device__ uint64_t *out_empty(int o) const { return bars() + 2 * C::kIn + C::kOut + o; }
     __device__ uint32_t *abort_flag() const {
-        return reinterpret_cast<uint32_t *>(base + (C::kStageBytes + C::kStageMeta) * C::kStages);
+        return reinterpret_cast<uint32_t *>(bars() + 2 * (C::kIn + C::kOut));
     }
     // first ring iteration that holds no tile (set once by the producer)
     __device__ uint32_t *end_iter() const { return abort_flag() + 1; }
@@ -113,22 +152,33 @@ __device__ __forceinline__ typename Op::T tile_elem(const uint32_t *buf, const t
 }
 
 template <class Op, bool INCL, class C>
-__global__ void __launch_bounds__(C::kThreads, C::kMinBlocks)
+__global__ void __launch_bounds__(C::kThreads, 1)
     scan_kernel(const typename Op::T *in, typename Op::T *out, uint64_t n, uint32_t num_tiles,
                 ScratchHeader *hdr, uint64_t *desc, FaultConfig fault) {
     using T = typename Op::T;
-    constexpr int NW = C::kWarps, ITEMS = C::kItems, STAGES = C::kStages, TILE = C::kTile;
+    constexpr int NW = C::kWarps, ITEMS = C::kItems, TILE = C::kTile;
+    constexpr int SIN = C::kIn, SOUT = C::kOut, RING = C::kRing, LW = C::kLookers;
     constexpr int WE = C::kWarpElems;
     constexpr uint32_t NCONS = C::kConsumers;
+    constexpr uint32_t kReducer0 = 1, kLooker0 = 1 + SIN, kReloader = 1 + SIN + LW,
+                       kConsumer0 = 2 + SIN + LW;
 
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const ScanSmem<C> sm(smem_raw);
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(sm.full(s), 1);
-            mbar_init(sm.carry_ready(s), 1);
-            mbar_init(sm.empty(s), NW);
+        for (int s = 0; s < SIN; ++s) {
+            mbar_init(sm.in_full(s), 1);
+            mbar_init(sm.in_empty(s), 1);
+        }
+        for (int o = 0; o < SOUT; ++o) {
+            mbar_init(sm.out_full(o), 1);
+            mbar_init(sm.out_empty(o), NW);
+        }
+        for (int i = 0; i < RING; ++i) {
+            mbar_init(sm.info_ready(i), 1);
+            mbar_init(sm.carry_ready(i), 1);
+            mbar_init(sm.info_free(i), NW);
         }
         *sm.abort_flag() = 0;
         *sm.end_iter() = kNoTile;
@@ -141,6 +191,9 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks)
         valid = rem < uint64_t(TILE) ? uint32_t(rem) : uint32_t(TILE);
         bulk = valid == uint32_t(TILE) ? valid : (valid & ~3u);
     };
+    auto stop_at = [&](uint32_t k) {  // no ring iteration from k on holds a tile
+        *reinterpret_cast<volatile uint32_t *>(sm.end_iter()) = k;
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------- producer
@@ -149,12 +202,13 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks)
         // ever waits for tiles that some running block already holds.
         if (lane != 0) return;
         for (uint32_t k = 0;; ++k) {
-            const int s = int(k % STAGES);
-            if (k >= STAGES && !mbar_wait(sm.empty(s), ((k / STAGES) - 1) & 1u, kPipeWaitLimit)) {
+            const int s = int(k % SIN), i = int(k % RING);
+            if ((k >= uint32_t(SIN) &&
+                 !mbar_wait(sm.in_empty(s), ((k / SIN) - 1) & 1u, kPipeWaitLimit)) ||
+                (k >= uint32_t(RING) &&
+                 !mbar_wait(sm.info_free(i), ((k / RING) - 1) & 1u, kPipeWaitLimit))) {
                 record_error(hdr, DWP_ERR_PIPELINE_TIMEOUT);
-                // the stage is still in use: leave it alone, and let every
-                // warp waiting for iteration k or later stop
-                *reinterpret_cast<volatile uint32_t *>(sm.end_iter()) = k - 1;
+                stop_at(k - 1);  // buffers still in use: leave them alone
                 return;
             }
             uint32_t t = kNoTile;
@@ -162,50 +216,49 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks)
                 t = atomicAdd(&hdr->tile_counter, 1u);
                 if (t >= num_tiles) t = kNoTile;
             }
-            *reinterpret_cast<volatile uint32_t *>(sm.tile_id(s)) = t;
+            *reinterpret_cast<volatile uint32_t *>(sm.tile_id(i)) = t;
             if (t == kNoTile) {
-                // iteration k carries the sentinel to its tile warp and the
-                // consumers; warps waiting for later iterations see end_iter
-                *reinterpret_cast<volatile uint32_t *>(sm.end_iter()) = k;
-                mbar_arrive(sm.full(s));
+                // iteration k carries the sentinel down the pipeline; warps
+                // waiting for later iterations see end_iter < their k
+                stop_at(k);
+                mbar_arrive(sm.in_full(s));
                 return;
             }
             uint32_t valid, bulk;
             tile_extent(t, valid, bulk);
-            const uint32_t bytes = bulk * 4u;
-            if (bytes) {
-                mbar_arrive_expect_tx(sm.full(s), bytes);
-                bulk_load(sm.data(s), in + uint64_t(t) * TILE, bytes, sm.full(s));
+            if (bulk) {
+                mbar_arrive_expect_tx(sm.in_full(s), bulk * 4u);
+                bulk_load_hint(sm.in_data(s), in + uint64_t(t) * TILE, bulk * 4u, sm.in_full(s),
+                               l2_policy_evict_last());
             } else {
-                mbar_arrive(sm.full(s));
+                mbar_arrive(sm.in_full(s));
             }
         }
     }
 
-    if (warp <= uint32_t(STAGES)) {
-        // ----------------------------------------------------- tile warps
-        const int s = int(warp) - 1;
-        bool draining = false;
+    if (warp >= kReducer0 && warp < kLooker0) {
+        // -------------------------------------------------------- reducers
+        const int s = int(warp - kReducer0);
         for (uint32_t use = 0;; ++use) {
-            const int w = warp_wait_or_end(sm.full(s), use & 1u, use * STAGES + uint32_t(s),
-                                           sm.end_iter());
+            const uint32_t k = use * SIN + uint32_t(s);
+            const int i = int(k % RING);
+            const int w = warp_wait_or_end(sm.in_full(s), use & 1u, k, sm.end_iter());
             if (w != 2) {
                 if (w == 0 && lane == 0) record_error(hdr, DWP_ERR_PIPELINE_TIMEOUT);
                 return;
             }
-            const uint32_t t = ld_volatile_smem(sm.tile_id(s));
+            const uint32_t t = ld_volatile_smem(sm.tile_id(i));
             if (t == kNoTile) {
-                if (lane == 0) mbar_arrive(sm.carry_ready(s));
+                if (lane == 0) mbar_arrive(sm.info_ready(i));
                 return;
             }
-            if (!draining && ld_volatile_smem(sm.abort_flag()) != 0) draining = true;
-            if (draining) {
-                // an earlier tile of this block gave up: poison this one so
-                // no successor waits for it, and let the consumers skip it
+            if (ld_volatile_smem(sm.abort_flag()) != 0) {
+                // an earlier tile of this block gave up: poison this one
                 if (lane == 0) {
                     st_relaxed_gpu(desc + t, make_desc(kPoison, 0u));
-                    *sm.lbres(s) = 1u;
-                    mbar_arrive(sm.carry_ready(s));
+                    *sm.lbres(i) = 1u;
+                    mbar_arrive(sm.in_empty(s));
+                    mbar_arrive(sm.info_ready(i));
                 }
                 __syncwarp();
                 continue;
@@ -213,17 +266,17 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks)
             uint32_t valid, bulk;
             tile_extent(t, valid, bulk);
             const uint64_t base = uint64_t(t) * TILE;
-            const uint32_t *buf = sm.data(s);
-            uint32_t *pre = sm.prefix(s);
-            uint32_t *lt = sm.lane_tot(s);
+            const uint32_t *buf = sm.in_data(s);
+            uint32_t *pre = sm.prefix(i);
+            uint32_t *lt = sm.lane_tot(i);
             // totals of consumer threads c = lane + 32*w, whose ITEMS
             // contiguous elements start at c*ITEMS
             T tot[NW];
             if (valid == uint32_t(TILE)) {
                 const uint4 *v4 = reinterpret_cast<const uint4 *>(buf);
 #pragma unroll
-                for (int w = 0; w < NW; ++w) {
-                    const uint32_t c = lane + 32u * w;
+                for (int w2 = 0; w2 < NW; ++w2) {
+                    const uint32_t c = lane + 32u * w2;
                     T acc = Op::identity();
 #pragma unroll
                     for (int v = 0; v < ITEMS / 4; ++v) {
@@ -231,23 +284,26 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks)
                         acc = Op::combine(acc, Op::combine(Op::combine(Op::from_bits(q.x), Op::from_bits(q.y)),
                                                            Op::combine(Op::from_bits(q.z), Op::from_bits(q.w))));
                     }
-                    tot[w] = acc;
+                    tot[w2] = acc;
                 }
             } else {
 #pragma unroll
-                for (int w = 0; w < NW; ++w) {
-                    const uint32_t c = lane + 32u * w;
+                for (int w2 = 0; w2 < NW; ++w2) {
+                    const uint32_t c = lane + 32u * w2;
                     T acc = Op::identity();
                     for (int j = 0; j < ITEMS; ++j)
                         acc = Op::combine(acc, tile_elem<Op>(buf, in, base, c * ITEMS + j, bulk, valid));
-                    tot[w] = acc;
+                    tot[w2] = acc;
                 }
             }
-#pragma unroll
-            for (int w = 0; w < NW; ++w) pre[prefix_slot(lane + 32u * w)] = Op::to_bits(tot[w]);
+            // the input stage is no longer needed
             __syncwarp();
-            // lane l scans the NW consecutive thread totals NW*l .. NW*l+NW-1
-            // (padded slots; for NW = 8 word 9l+j, banks all distinct) ...
+            if (lane == 0) mbar_arrive(sm.in_empty(s));
+#pragma unroll
+            for (int w2 = 0; w2 < NW; ++w2) pre[prefix_slot(lane + 32u * w2)] = Op::to_bits(tot[w2]);
+            __syncwarp();
+            // lane l scans the PER consecutive thread totals PER*l .. (padded
+            // slots; for PER = 8 words 9l+j, banks all distinct) ...
             constexpr int PER = NCONS / 32;
             T mine[PER];
             T run = Op::identity();
@@ -271,51 +327,118 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks)
             for (int j = 0; j < PER; ++j)
                 pre[prefix_slot(lane * PER + j)] = Op::to_bits(Op::combine(lane_excl, mine[j]));
             // publish the aggregate at once (tile 0: its inclusive prefix)
-            if (lane == 0 && t != fault.never_publish_tile)
-                st_relaxed_gpu(desc + t, make_desc(t == 0 ? kPrefix : kAggregate, Op::to_bits(agg)));
-            // grid layer
+            if (lane == 0) {
+                if (t != fault.never_publish_tile)
+                    st_relaxed_gpu(desc + t, make_desc(t == 0 ? kPrefix : kAggregate, Op::to_bits(agg)));
+                *sm.agg(i) = Op::to_bits(agg);
+                *sm.lbres(i) = 0u;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sm.info_ready(i));
+        }
+    }
+
+    if (warp >= kLooker0 && warp < kReloader) {
+        // --------------------------------------------------- look-back warps
+        const uint32_t j = warp - kLooker0;
+        bool draining = false;
+        for (uint32_t k = j;; k += LW) {
+            const int i = int(k % RING);
+            const int w = warp_wait_or_end(sm.info_ready(i), (k / RING) & 1u, k, sm.end_iter());
+            if (w != 2) {
+                if (w == 0 && lane == 0) record_error(hdr, DWP_ERR_PIPELINE_TIMEOUT);
+                return;
+            }
+            const uint32_t t = ld_volatile_smem(sm.tile_id(i));
+            if (t == kNoTile) {
+                if (lane == 0) mbar_arrive(sm.carry_ready(i));
+                return;
+            }
+            if (!draining && ld_volatile_smem(sm.abort_flag()) != 0) draining = true;
             T carry = Op::identity();
-            int rc = 0;
-            if (t != 0)
-                rc = lookback<Op, C::kLookK>(desc, t, lane, fault.spin_limit, sm.lb_scratch(s), &carry);
+            int rc = (draining || ld_volatile_smem(sm.lbres(i)) != 0u) ? 1 : 0;
+            if (rc == 0 && t != 0)
+                rc = lookback<Op, C::kLookK>(desc, t, lane, fault.spin_limit, sm.lb_scratch(i), &carry);
             if (lane == 0) {
                 if (rc == 0) {
                     if (t != 0 && t != fault.never_publish_tile)
-                        st_relaxed_gpu(desc + t, make_desc(kPrefix, Op::to_bits(Op::combine(carry, agg))));
+                        st_relaxed_gpu(desc + t, make_desc(kPrefix, Op::to_bits(Op::combine(carry, Op::from_bits(*sm.agg(i))))));
                 } else {
                     // give up on this tile: poison it so no successor waits
                     st_relaxed_gpu(desc + t, make_desc(kPoison, 0u));
                     if (rc == 2) record_error(hdr, DWP_ERR_LOOKBACK_TIMEOUT);
                     *reinterpret_cast<volatile uint32_t *>(sm.abort_flag()) = 1u;
                 }
-                *sm.carry(s) = Op::to_bits(carry);
-                *sm.lbres(s) = uint32_t(rc);
+                *sm.carry(i) = Op::to_bits(carry);
+                *sm.lbres(i) = uint32_t(rc);
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(sm.carry_ready(s));
+            if (lane == 0) mbar_arrive(sm.carry_ready(i));
             if (rc != 0) draining = true;
         }
     }
 
+    if (warp == kReloader) {
+        // ---------------------------------------------------------- reloader
+        if (lane != 0) return;
+        for (uint32_t k = 0;; ++k) {
+            const int i = int(k % RING), o = int(k % SOUT);
+            // carry_ready(k) is a single-lane wait here; end_iter as above
+            int w = 0;
+            for (uint32_t p = 0; p < kPipeWaitLimit; ++p) {
+                if (mbar_try_wait(sm.carry_ready(i), (k / RING) & 1u)) { w = 2; break; }
+                if (ld_volatile_smem(sm.end_iter()) < k) { w = 1; break; }
+                if (p >= 8) __nanosleep(64);
+            }
+            if (w == 2 && k >= uint32_t(SOUT) &&
+                !mbar_wait(sm.out_empty(o), ((k / SOUT) - 1) & 1u, kPipeWaitLimit))
+                w = 0;
+            if (w != 2) {
+                if (w == 0) record_error(hdr, DWP_ERR_PIPELINE_TIMEOUT);
+                return;
+            }
+            const uint32_t t = ld_volatile_smem(sm.tile_id(i));
+            if (t == kNoTile || ld_volatile_smem(sm.lbres(i)) != 0u) {
+                mbar_arrive(sm.out_full(o));
+                if (t == kNoTile) return;
+                continue;
+            }
+            uint32_t valid, bulk;
+            tile_extent(t, valid, bulk);
+            if (bulk) {
+                mbar_arrive_expect_tx(sm.out_full(o), bulk * 4u);
+                bulk_load_hint(sm.out_data(o), in + uint64_t(t) * TILE, bulk * 4u, sm.out_full(o),
+                               l2_policy_evict_first());
+            } else {
+                mbar_arrive(sm.out_full(o));
+            }
+        }
+    }
+
+    if (warp < kConsumer0) return;
     // ---------------------------------------------------------- consumers
-    const uint32_t cw = warp - 1 - STAGES;
+    // Consumer warp w owns chunk w of every tile; thread c = 32w + lane owns
+    // ITEMS contiguous elements and needs no cross-thread step: its in-tile
+    // exclusive prefix comes from the reducer, the carry from the look-back.
+    const uint32_t cw = warp - kConsumer0;
     const uint32_t c = cw * 32 + lane;
-    int pending = -1;  // lane 0: stage whose bulk store may still read smem
+    int pending = -1;  // lane 0: output stage whose bulk store may still read smem
     for (uint32_t k = 0;; ++k) {
-        const int s = int(k % STAGES);
-        const uint32_t par = (k / STAGES) & 1u;
-        const int w = warp_wait_or_end(sm.full(s), par, k, sm.end_iter());
-        if (w != 2 || !warp_wait(sm.carry_ready(s), par)) {
-            if (w != 1 && lane == 0) record_error(hdr, DWP_ERR_PIPELINE_TIMEOUT);
+        const int i = int(k % RING), o = int(k % SOUT);
+        const int w = warp_wait_or_end(sm.out_full(o), (k / SOUT) & 1u, k, sm.end_iter());
+        if (w != 2) {
+            if (w == 0 && lane == 0) record_error(hdr, DWP_ERR_PIPELINE_TIMEOUT);
             break;
         }
-        const uint32_t t = ld_volatile_smem(sm.tile_id(s));
+        const uint32_t t = ld_volatile_smem(sm.tile_id(i));
         if (t == kNoTile) break;
-        if (ld_volatile_smem(sm.lbres(s)) != 0u) {
+        if (ld_volatile_smem(sm.lbres(i)) != 0u) {
+            __syncwarp();
             if (lane == 0) {
+                mbar_arrive(sm.info_free(i));
                 bulk_wait_read<0>();
-                if (pending >= 0) mbar_arrive(sm.empty(pending));
-                mbar_arrive(sm.empty(s));
+                if (pending >= 0) mbar_arrive(sm.out_empty(pending));
+                mbar_arrive(sm.out_empty(o));
                 pending = -1;
             }
             __syncwarp();
@@ -324,9 +447,11 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks)
         uint32_t valid, bulk;
         tile_extent(t, valid, bulk);
         const uint64_t base = uint64_t(t) * TILE;
-        uint32_t *buf = sm.data(s);
+        uint32_t *buf = sm.out_data(o);
         const uint32_t p0 = c * ITEMS;  // this thread's first element
-        T acc = Op::combine(Op::from_bits(*sm.carry(s)), Op::from_bits(sm.prefix(s)[prefix_slot(c)]));
+        T acc = Op::combine(Op::from_bits(*sm.carry(i)), Op::from_bits(sm.prefix(i)[prefix_slot(c)]));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sm.info_free(i));  // the info slot has been read
         if (valid == uint32_t(TILE)) {
             uint4 *v4 = reinterpret_cast<uint4 *>(buf + p0);
 #pragma unroll
@@ -371,15 +496,15 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks)
             const uint32_t w0 = cw * WE;
             const uint32_t w1 = min(w0 + uint32_t(WE), bulk);
             if (w1 > w0) {
-                bulk_store(out + base + w0, buf + w0, (w1 - w0) * 4u);
+                bulk_store_hint(out + base + w0, buf + w0, (w1 - w0) * 4u, l2_policy_evict_first());
                 bulk_commit();
                 bulk_wait_read<1>();
-                if (pending >= 0) mbar_arrive(sm.empty(pending));
-                pending = s;
+                if (pending >= 0) mbar_arrive(sm.out_empty(pending));
+                pending = o;
             } else {
                 bulk_wait_read<0>();
-                if (pending >= 0) mbar_arrive(sm.empty(pending));
-                mbar_arrive(sm.empty(s));
+                if (pending >= 0) mbar_arrive(sm.out_empty(pending));
+                mbar_arrive(sm.out_empty(o));
                 pending = -1;
             }
         }
