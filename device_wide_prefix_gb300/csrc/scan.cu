@@ -80,10 +80,10 @@ struct ScanConfig {
 #define DWP_SCAN_WARPS 8
 #endif
 #ifndef DWP_SCAN_ITEMS
-#define DWP_SCAN_ITEMS 20
+#define DWP_SCAN_ITEMS 28
 #endif
 #ifndef DWP_SCAN_IN
-#define DWP_SCAN_IN 5
+#define DWP_SCAN_IN 3
 #endif
 #ifndef DWP_SCAN_OUT
 #define DWP_SCAN_OUT 4
@@ -95,7 +95,7 @@ struct ScanConfig {
 #define DWP_SCAN_LOOKERS 8
 #endif
 #ifndef DWP_SCAN_LOOKK
-#define DWP_SCAN_LOOKK 4
+#define DWP_SCAN_LOOKK 1
 #endif
 using ScanCfg = ScanConfig<DWP_SCAN_WARPS, DWP_SCAN_ITEMS, DWP_SCAN_IN, DWP_SCAN_OUT,
                            DWP_SCAN_RING, DWP_SCAN_LOOKERS, DWP_SCAN_LOOKK>;
