@@ -10,17 +10,20 @@
 // an associative, non-commutative operator.
 //
 // The pipeline is the plain scan's (scan.cu): producer warp with bulk loads
-// into a ring of stages, one tile warp per stage, consumer warps with
+// into SIN input stages; reducer warps that free their input stage as soon
+// as the tile is reduced; a pool of look-back warps; a reloader warp that
+// brings a tile back from L2 once its carry is known; consumer warps with
 // per-warp bulk stores.  What differs:
-//   * the tile warp first marks the heads of its tile (every offset value in
-//     [tile start, tile end)) in a shared-memory bitmap.  It finds the first
-//     offset at or after the tile start in a per-block sample of the offsets
-//     held in shared memory (exact when N + 1 <= kSample, the skewed-length
-//     workload's case), else by a warp-wide 32-ary search of global memory
-//     inside the sampled interval; then it walks the offsets of the tile;
+//   * the reducer first marks the heads of its tile (every offset value in
+//     [tile start, tile end)) in a bitmap kept in the tile's info slot.  It
+//     finds the first offset at or after the tile start in a per-block
+//     sample of the offsets held in shared memory (exact when N + 1 <=
+//     kSample, the skewed-length workload's case), else by a warp-wide
+//     32-ary search of global memory inside the sampled interval; then it
+//     walks the offsets of the tile;
 //   * per-thread totals and their exclusive prefix are (head, value) pairs;
 //   * a tile holding a head publishes its inclusive prefix at once (its value
-//     after its last head is final); the look-back then is a plain u32-add
+//     after its last head is final); the look-back is a plain u32-add
 //     look-back that stops at the nearest prefix, and runs only if the
 //     tile's first row is not itself a head;
 //   * rows outside [offsets[0], min(offsets[N], n)) are not written.
@@ -37,68 +40,105 @@ namespace {
 
 constexpr int kSample = 2048;  // offsets sampled into shared memory per block
 
-template <int NW_, int ITEMS_, int STAGES_, int LOOKK_>
+template <int NW_, int ITEMS_, int SIN_, int SOUT_, int RING_, int LW_, int LOOKK_>
 struct SegConfig {
     static constexpr int kWarps = NW_;
     static constexpr int kItems = ITEMS_;
-    static constexpr int kStages = STAGES_;
+    static constexpr int kIn = SIN_;
+    static constexpr int kOut = SOUT_;
+    static constexpr int kRing = RING_;
+    static constexpr int kLookers = LW_;
     static constexpr int kLookK = LOOKK_;
-    static constexpr int kThreads = (1 + STAGES_ + NW_) * 32;
+    static constexpr int kThreads = (2 + SIN_ + LW_ + NW_) * 32;
     static constexpr int kConsumers = NW_ * 32;
     static constexpr int kWarpElems = 32 * ITEMS_;
     static constexpr int kTile = NW_ * 32 * ITEMS_;
     static_assert(ITEMS_ % 4 == 0 && (ITEMS_ / 4) % 2 == 1, "ITEMS must be an odd multiple of 4");
     static_assert(ITEMS_ <= 32, "a thread's head bits span at most two bitmap words");
     static_assert(NW_ >= 1 && NW_ <= 32, "");
+    static_assert(RING_ % LW_ == 0, "a look-back warp must own every use of its info slots");
+    static_assert(SOUT_ >= 2, "the reloader waits for the output stage of iteration k - SOUT");
     static constexpr size_t kStageBytes = size_t(kTile) * 4;
     static constexpr int kPrefixWords = kConsumers + kConsumers / 8;
+    static constexpr int kPHeadWords = kConsumers / 4;  // one head byte per consumer thread
     static constexpr int kHeadWords = kTile / 32 + 1;   // tile head bitmap (+1 spill word)
-    static constexpr int kPHeadWords = kConsumers / 4;   // one head byte per consumer thread
-    // mbarriers 32 B; tile id, carry, look-back result, pad 16 B; prefixes;
-    // prefix head bits; tile head bitmap; lane totals 33 + lane head bits 33
-    static constexpr size_t kStageMeta =
-        48 + 4 * (kPrefixWords + kPHeadWords + kHeadWords + 66 + 33);
-    // + abort, end, lo, hi words + the offset sample
-    static constexpr size_t kSmemBytes = (kStageBytes + kStageMeta) * kStages + 16 + 4 * kSample;
+    // info slot: 3 mbarriers + pad (32 B); tile id, aggregate, carry,
+    // look-back result, aggregate head, first-row head, pad x2 (32 B);
+    // prefix values; prefix head bytes; head bitmap; lane totals 33; lane
+    // heads 33; look-back scratch 33
+    static constexpr size_t kInfoBytes =
+        64 + 4 * (kPrefixWords + kPHeadWords + kHeadWords + 33 + 33 + 33);
+    static_assert(kInfoBytes % 8 == 0, "info slots hold mbarriers");
+    static constexpr size_t kBarBytes = 16 * (SIN_ + SOUT_);
+    // + abort, end, cover lo, cover hi, then the offset sample
+    static constexpr size_t kSmemBytes = kStageBytes * (SIN_ + SOUT_) + kInfoBytes * RING_ +
+                                         kBarBytes + 16 + 4 * kSample;
 };
 
 #ifndef DWP_SEG_WARPS
-#define DWP_SEG_WARPS 16
+#define DWP_SEG_WARPS 8
 #endif
 #ifndef DWP_SEG_ITEMS
-#define DWP_SEG_ITEMS 20
+#define DWP_SEG_ITEMS 28
 #endif
-#ifndef DWP_SEG_STAGES
-#define DWP_SEG_STAGES 4
+#ifndef DWP_SEG_IN
+#define DWP_SEG_IN 3
 #endif
-using SegCfg = SegConfig<DWP_SEG_WARPS, DWP_SEG_ITEMS, DWP_SEG_STAGES, 4>;
+#ifndef DWP_SEG_OUT
+#define DWP_SEG_OUT 3
+#endif
+#ifndef DWP_SEG_RING
+#define DWP_SEG_RING 12
+#endif
+#ifndef DWP_SEG_LOOKERS
+#define DWP_SEG_LOOKERS 6
+#endif
+#ifndef DWP_SEG_LOOKK
+#define DWP_SEG_LOOKK 1
+#endif
+using SegCfg = SegConfig<DWP_SEG_WARPS, DWP_SEG_ITEMS, DWP_SEG_IN, DWP_SEG_OUT, DWP_SEG_RING,
+                         DWP_SEG_LOOKERS, DWP_SEG_LOOKK>;
 
 template <class C>
 struct SegSmem {
     unsigned char *base;
     __device__ explicit SegSmem(unsigned char *p) : base(p) {}
-    __device__ uint32_t *data(int s) const {
+    __device__ uint32_t *in_data(int s) const {
         return reinterpret_cast<uint32_t *>(base + size_t(s) * C::kStageBytes);
     }
-    __device__ unsigned char *meta(int s) const {
-        return base + C::kStageBytes * C::kStages + size_t(s) * C::kStageMeta;
+    __device__ uint32_t *out_data(int o) const {
+        return reinterpret_cast<uint32_t *>(base + size_t(C::kIn + o) * C::kStageBytes);
     }
-    __device__ uint64_t *full(int s) const { return reinterpret_cast<uint64_t *>(meta(s)); }
-    __device__ uint64_t *carry_ready(int s) const { return full(s) + 1; }
-    __device__ uint64_t *empty(int s) const { return full(s) + 2; }
-    __device__ uint32_t *tile_id(int s) const { return reinterpret_cast<uint32_t *>(meta(s) + 32); }
-    __device__ uint32_t *carry(int s) const { return tile_id(s) + 1; }
-    __device__ uint32_t *lbres(int s) const { return tile_id(s) + 2; }
-    __device__ uint32_t *prefix(int s) const { return tile_id(s) + 4; }
-    __device__ unsigned char *phead(int s) const {
-        return reinterpret_cast<unsigned char *>(prefix(s) + C::kPrefixWords);
+    __device__ unsigned char *info(int i) const {
+        return base + C::kStageBytes * (C::kIn + C::kOut) + size_t(i) * C::kInfoBytes;
     }
-    __device__ uint32_t *heads(int s) const { return prefix(s) + C::kPrefixWords + C::kPHeadWords; }
-    __device__ uint32_t *lane_tot(int s) const { return heads(s) + C::kHeadWords; }
-    __device__ uint32_t *lane_head(int s) const { return lane_tot(s) + 33; }
-    __device__ uint32_t *lb_scratch(int s) const { return lane_head(s) + 33; }
+    __device__ uint64_t *info_ready(int i) const { return reinterpret_cast<uint64_t *>(info(i)); }
+    __device__ uint64_t *carry_ready(int i) const { return info_ready(i) + 1; }
+    __device__ uint64_t *info_free(int i) const { return info_ready(i) + 2; }
+    __device__ uint32_t *tile_id(int i) const { return reinterpret_cast<uint32_t *>(info(i) + 32); }
+    __device__ uint32_t *agg(int i) const { return tile_id(i) + 1; }
+    __device__ uint32_t *carry(int i) const { return tile_id(i) + 2; }
+    __device__ uint32_t *lbres(int i) const { return tile_id(i) + 3; }
+    __device__ uint32_t *agg_head(int i) const { return tile_id(i) + 4; }
+    __device__ uint32_t *first_head(int i) const { return tile_id(i) + 5; }
+    __device__ uint32_t *prefix(int i) const { return tile_id(i) + 8; }
+    __device__ unsigned char *phead(int i) const {
+        return reinterpret_cast<unsigned char *>(prefix(i) + C::kPrefixWords);
+    }
+    __device__ uint32_t *heads(int i) const { return prefix(i) + C::kPrefixWords + C::kPHeadWords; }
+    __device__ uint32_t *lane_tot(int i) const { return heads(i) + C::kHeadWords; }
+    __device__ uint32_t *lane_head(int i) const { return lane_tot(i) + 33; }
+    __device__ uint32_t *lb_scratch(int i) const { return lane_head(i) + 33; }
+    __device__ uint64_t *bars() const {
+        return reinterpret_cast<uint64_t *>(base + C::kStageBytes * (C::kIn + C::kOut) +
+                                            C::kInfoBytes * C::kRing);
+    }
+    __device__ uint64_t *in_full(int s) const { return bars() + s; }
+    __device__ uint64_t *in_empty(int s) const { return bars() + C::kIn + s; }
+    __device__ uint64_t *out_full(int o) const { return bars() + 2 * C::kIn + o; }
+    __device__ uint64_t *out_empty(int o) const { return bars() + 2 * C::kIn + C::kOut + o; }
     __device__ uint32_t *words() const {
-        return reinterpret_cast<uint32_t *>(base + (C::kStageBytes + C::kStageMeta) * C::kStages);
+        return reinterpret_cast<uint32_t *>(bars() + 2 * (C::kIn + C::kOut));
     }
     __device__ uint32_t *abort_flag() const { return words(); }
     __device__ uint32_t *end_iter() const { return words() + 1; }
@@ -149,9 +189,12 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                    uint64_t n, uint32_t num_tiles, ScratchHeader *hdr, uint64_t *desc,
                    FaultConfig fault) {
     using Op = OpU32Add;
-    constexpr int NW = C::kWarps, ITEMS = C::kItems, STAGES = C::kStages, TILE = C::kTile;
+    constexpr int NW = C::kWarps, ITEMS = C::kItems, TILE = C::kTile;
+    constexpr int SIN = C::kIn, SOUT = C::kOut, RING = C::kRing, LW = C::kLookers;
     constexpr int WE = C::kWarpElems;
     constexpr uint32_t NCONS = C::kConsumers;
+    constexpr uint32_t kReducer0 = 1, kLooker0 = 1 + SIN, kReloader = 1 + SIN + LW,
+                       kConsumer0 = 2 + SIN + LW;
 
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const SegSmem<C> sm(smem_raw);
@@ -164,10 +207,18 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     for (uint32_t i = threadIdx.x; i < nsample; i += blockDim.x)
         sm.sample()[i] = __ldg(off + min(uint64_t(i) * stride, uint64_t(nseg)));
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(sm.full(s), 1);
-            mbar_init(sm.carry_ready(s), 1);
-            mbar_init(sm.empty(s), NW);
+        for (int s = 0; s < SIN; ++s) {
+            mbar_init(sm.in_full(s), 1);
+            mbar_init(sm.in_empty(s), 1);
+        }
+        for (int o = 0; o < SOUT; ++o) {
+            mbar_init(sm.out_full(o), 1);
+            mbar_init(sm.out_empty(o), NW);
+        }
+        for (int i = 0; i < RING; ++i) {
+            mbar_init(sm.info_ready(i), 1);
+            mbar_init(sm.carry_ready(i), 1);
+            mbar_init(sm.info_free(i), NW);
         }
         *sm.abort_flag() = 0;
         *sm.end_iter() = kNoTile;
@@ -183,15 +234,19 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         valid = rem < uint64_t(TILE) ? uint32_t(rem) : uint32_t(TILE);
         bulk = valid == uint32_t(TILE) ? valid : (valid & ~3u);
     };
+    auto stop_at = [&](uint32_t k) { *reinterpret_cast<volatile uint32_t *>(sm.end_iter()) = k; };
 
     if (warp == 0) {
         // ------------------------------------------------------- producer
         if (lane != 0) return;
         for (uint32_t k = 0;; ++k) {
-            const int s = int(k % STAGES);
-            if (k >= STAGES && !mbar_wait(sm.empty(s), ((k / STAGES) - 1) & 1u, kPipeWaitLimit)) {
+            const int s = int(k % SIN), i = int(k % RING);
+            if ((k >= uint32_t(SIN) &&
+                 !mbar_wait(sm.in_empty(s), ((k / SIN) - 1) & 1u, kPipeWaitLimit)) ||
+                (k >= uint32_t(RING) &&
+                 !mbar_wait(sm.info_free(i), ((k / RING) - 1) & 1u, kPipeWaitLimit))) {
                 record_error(hdr, DWP_ERR_PIPELINE_TIMEOUT);
-                *reinterpret_cast<volatile uint32_t *>(sm.end_iter()) = k - 1;
+                stop_at(k - 1);
                 return;
             }
             uint32_t t = kNoTile;
@@ -199,45 +254,46 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 t = atomicAdd(&hdr->tile_counter, 1u);
                 if (t >= num_tiles) t = kNoTile;
             }
-            *reinterpret_cast<volatile uint32_t *>(sm.tile_id(s)) = t;
+            *reinterpret_cast<volatile uint32_t *>(sm.tile_id(i)) = t;
             if (t == kNoTile) {
-                *reinterpret_cast<volatile uint32_t *>(sm.end_iter()) = k;
-                mbar_arrive(sm.full(s));
+                stop_at(k);
+                mbar_arrive(sm.in_full(s));
                 return;
             }
             uint32_t valid, bulk;
             tile_extent(t, valid, bulk);
             if (bulk) {
-                mbar_arrive_expect_tx(sm.full(s), bulk * 4u);
-                bulk_load(sm.data(s), in + uint64_t(t) * TILE, bulk * 4u, sm.full(s));
+                mbar_arrive_expect_tx(sm.in_full(s), bulk * 4u);
+                bulk_load_hint(sm.in_data(s), in + uint64_t(t) * TILE, bulk * 4u, sm.in_full(s),
+                               l2_policy_evict_last());
             } else {
-                mbar_arrive(sm.full(s));
+                mbar_arrive(sm.in_full(s));
             }
         }
     }
 
-    if (warp <= uint32_t(STAGES)) {
-        // ----------------------------------------------------- tile warps
-        const int s = int(warp) - 1;
-        bool draining = false;
+    if (warp >= kReducer0 && warp < kLooker0) {
+        // -------------------------------------------------------- reducers
+        const int s = int(warp - kReducer0);
         for (uint32_t use = 0;; ++use) {
-            const int w = warp_wait_or_end(sm.full(s), use & 1u, use * STAGES + uint32_t(s),
-                                           sm.end_iter());
+            const uint32_t k = use * SIN + uint32_t(s);
+            const int i = int(k % RING);
+            const int w = warp_wait_or_end(sm.in_full(s), use & 1u, k, sm.end_iter());
             if (w != 2) {
                 if (w == 0 && lane == 0) record_error(hdr, DWP_ERR_PIPELINE_TIMEOUT);
                 return;
             }
-            const uint32_t t = ld_volatile_smem(sm.tile_id(s));
+            const uint32_t t = ld_volatile_smem(sm.tile_id(i));
             if (t == kNoTile) {
-                if (lane == 0) mbar_arrive(sm.carry_ready(s));
+                if (lane == 0) mbar_arrive(sm.info_ready(i));
                 return;
             }
-            if (!draining && ld_volatile_smem(sm.abort_flag()) != 0) draining = true;
-            if (draining) {
+            if (ld_volatile_smem(sm.abort_flag()) != 0) {
                 if (lane == 0) {
                     st_relaxed_gpu(desc + t, make_desc(kPoison, 0u));
-                    *sm.lbres(s) = 1u;
-                    mbar_arrive(sm.carry_ready(s));
+                    *sm.lbres(i) = 1u;
+                    mbar_arrive(sm.in_empty(s));
+                    mbar_arrive(sm.info_ready(i));
                 }
                 __syncwarp();
                 continue;
@@ -246,14 +302,13 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             tile_extent(t, valid, bulk);
             const uint64_t base = uint64_t(t) * TILE;
             const uint64_t tend = base + valid;
-            uint32_t *heads = sm.heads(s);
+            uint32_t *heads = sm.heads(i);
 
             // -- S1: heads of this tile ------------------------------------
-            for (int i = int(lane); i < C::kHeadWords; i += 32) heads[i] = 0u;
+            for (int q = int(lane); q < C::kHeadWords; q += 32) heads[q] = 0u;
             __syncwarp();
-            // last sampled offset below the tile start (sample 0 may not be)
             const uint32_t *smp = sm.sample();
-            uint32_t a = 0, b = nsample;  // first sample >= base, by binary search
+            uint32_t a = 0, b = nsample;  // first sample >= base
             while (a < b) {
                 const uint32_t m = (a + b) >> 1;
                 if (uint64_t(smp[m]) < base) a = m + 1; else b = m;
@@ -268,28 +323,25 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 const uint32_t hi = uint32_t(min(uint64_t(a) * stride, uint64_t(nseg) + 1));
                 k0 = warp_lower_bound(off, lo, hi, uint32_t(base), lane);
             }
-            // walk the offsets inside [base, tend)
-            for (uint32_t k = k0; k <= nseg; k += 32) {
-                const uint64_t idx = uint64_t(k) + lane;
+            for (uint32_t kk = k0; kk <= nseg; kk += 32) {
+                const uint64_t idx = uint64_t(kk) + lane;
                 uint32_t p = 0xffffffffu;
                 if (idx <= nseg) p = stride == 1u ? smp[idx] : __ldg(off + idx);
-                const bool inside = idx <= nseg && uint64_t(p) >= base && uint64_t(p) < tend;
-                if (inside) {
+                if (idx <= nseg && uint64_t(p) >= base && uint64_t(p) < tend) {
                     const uint32_t r = uint32_t(uint64_t(p) - base);
                     atomicOr(&heads[r >> 5], 1u << (r & 31u));
                 }
-                // stop once some offset in this batch reached the tile end
                 if (__any_sync(0xffffffffu, idx > nseg || uint64_t(p) >= tend)) break;
             }
             __syncwarp();
 
             // -- per-thread (head, value) totals ---------------------------
-            const uint32_t *buf = sm.data(s);
-            uint32_t *pre = sm.prefix(s);
-            unsigned char *ph = sm.phead(s);
+            const uint32_t *buf = sm.in_data(s);
+            uint32_t *pre = sm.prefix(i);
+            unsigned char *ph = sm.phead(i);
 #pragma unroll
-            for (int w = 0; w < NW; ++w) {
-                const uint32_t c = lane + 32u * w;
+            for (int w2 = 0; w2 < NW; ++w2) {
+                const uint32_t c = lane + 32u * w2;
                 const uint32_t hb = head_bits(heads, c * ITEMS, ITEMS);
                 uint32_t acc = 0;
                 if (valid == uint32_t(TILE)) {
@@ -313,7 +365,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 pre[prefix_slot(c)] = acc;
                 ph[c] = hb ? 1 : 0;
             }
+            // the input stage is no longer needed
             __syncwarp();
+            if (lane == 0) mbar_arrive(sm.in_empty(s));
             // lane l scans threads PER*l .. PER*l+PER-1 with the pair operator
             constexpr int PER = NCONS / 32;
             uint32_t mv[PER], mh = 0, rv = 0, rh = 0;
@@ -327,13 +381,13 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 rv = hv ? v : rv + v;
                 rh |= hv;
             }
-            sm.lane_tot(s)[lane] = rv;
-            sm.lane_head(s)[lane] = rh;
+            sm.lane_tot(i)[lane] = rv;
+            sm.lane_head(i)[lane] = rh;
             __syncwarp();
             uint32_t ev = 0, eh = 0, av = 0, ah = 0;  // lane exclusive pair, tile aggregate
 #pragma unroll
             for (int l = 0; l < 32; ++l) {
-                const uint32_t v = sm.lane_tot(s)[l], h = sm.lane_head(s)[l];
+                const uint32_t v = sm.lane_tot(i)[l], h = sm.lane_head(i)[l];
                 if (uint32_t(l) < lane) {
                     ev = h ? v : ev + v;
                     eh |= h;
@@ -349,48 +403,109 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 pre[prefix_slot(lane * PER + j)] = hj ? mv[j] : ev + mv[j];
                 ph[lane * PER + j] = (hj | eh) ? 1 : 0;
             }
+            if (lane == 0) {
+                if (t != fault.never_publish_tile)
+                    st_relaxed_gpu(desc + t, make_desc((t == 0 || ah) ? kPrefix : kAggregate, av));
+                *sm.agg(i) = av;
+                *sm.agg_head(i) = ah;
+                *sm.first_head(i) = heads[0] & 1u;
+                *sm.lbres(i) = 0u;
+            }
             __syncwarp();
-            // -- publish, look back ------------------------------------------
-            const bool first_is_head = (heads[0] & 1u) != 0u;
-            if (lane == 0 && t != fault.never_publish_tile)
-                st_relaxed_gpu(desc + t,
-                               make_desc((t == 0 || ah) ? kPrefix : kAggregate, av));
+            if (lane == 0) mbar_arrive(sm.info_ready(i));
+        }
+    }
+
+    if (warp >= kLooker0 && warp < kReloader) {
+        // --------------------------------------------------- look-back warps
+        const uint32_t j = warp - kLooker0;
+        bool draining = false;
+        for (uint32_t k = j;; k += LW) {
+            const int i = int(k % RING);
+            const int w = warp_wait_or_end(sm.info_ready(i), (k / RING) & 1u, k, sm.end_iter());
+            if (w != 2) {
+                if (w == 0 && lane == 0) record_error(hdr, DWP_ERR_PIPELINE_TIMEOUT);
+                return;
+            }
+            const uint32_t t = ld_volatile_smem(sm.tile_id(i));
+            if (t == kNoTile) {
+                if (lane == 0) mbar_arrive(sm.carry_ready(i));
+                return;
+            }
+            if (!draining && ld_volatile_smem(sm.abort_flag()) != 0) draining = true;
             uint32_t carry = 0;
-            int rc = 0;
-            if (t != 0 && !first_is_head)
-                rc = lookback<Op, C::kLookK>(desc, t, lane, fault.spin_limit, sm.lb_scratch(s), &carry);
+            int rc = (draining || ld_volatile_smem(sm.lbres(i)) != 0u) ? 1 : 0;
+            const bool ah = ld_volatile_smem(sm.agg_head(i)) != 0u;
+            if (rc == 0 && t != 0 && ld_volatile_smem(sm.first_head(i)) == 0u)
+                rc = lookback<Op, C::kLookK>(desc, t, lane, fault.spin_limit, sm.lb_scratch(i), &carry);
             if (lane == 0) {
                 if (rc == 0) {
                     if (t != 0 && !ah && t != fault.never_publish_tile)
-                        st_relaxed_gpu(desc + t, make_desc(kPrefix, carry + av));
+                        st_relaxed_gpu(desc + t, make_desc(kPrefix, carry + *sm.agg(i)));
                 } else {
                     st_relaxed_gpu(desc + t, make_desc(kPoison, 0u));
                     if (rc == 2) record_error(hdr, DWP_ERR_LOOKBACK_TIMEOUT);
                     *reinterpret_cast<volatile uint32_t *>(sm.abort_flag()) = 1u;
                 }
-                *sm.carry(s) = carry;
-                *sm.lbres(s) = uint32_t(rc);
+                *sm.carry(i) = carry;
+                *sm.lbres(i) = uint32_t(rc);
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(sm.carry_ready(s));
+            if (lane == 0) mbar_arrive(sm.carry_ready(i));
             if (rc != 0) draining = true;
         }
     }
 
+    if (warp == kReloader) {
+        // ---------------------------------------------------------- reloader
+        if (lane != 0) return;
+        for (uint32_t k = 0;; ++k) {
+            const int i = int(k % RING), o = int(k % SOUT);
+            int w = 0;
+            for (uint32_t p = 0; p < kPipeWaitLimit; ++p) {
+                if (mbar_try_wait(sm.carry_ready(i), (k / RING) & 1u)) { w = 2; break; }
+                if (ld_volatile_smem(sm.end_iter()) < k) { w = 1; break; }
+                if (p >= 8) __nanosleep(64);
+            }
+            if (w == 2 && k >= uint32_t(SOUT) &&
+                !mbar_wait(sm.out_empty(o), ((k / SOUT) - 1) & 1u, kPipeWaitLimit))
+                w = 0;
+            if (w != 2) {
+                if (w == 0) record_error(hdr, DWP_ERR_PIPELINE_TIMEOUT);
+                return;
+            }
+            const uint32_t t = ld_volatile_smem(sm.tile_id(i));
+            if (t == kNoTile || ld_volatile_smem(sm.lbres(i)) != 0u) {
+                mbar_arrive(sm.out_full(o));
+                if (t == kNoTile) return;
+                continue;
+            }
+            uint32_t valid, bulk;
+            tile_extent(t, valid, bulk);
+            if (bulk) {
+                mbar_arrive_expect_tx(sm.out_full(o), bulk * 4u);
+                bulk_load_hint(sm.out_data(o), in + uint64_t(t) * TILE, bulk * 4u, sm.out_full(o),
+                               l2_policy_evict_first());
+            } else {
+                mbar_arrive(sm.out_full(o));
+            }
+        }
+    }
+
+    if (warp < kConsumer0) return;
     // ---------------------------------------------------------- consumers
-    const uint32_t cw = warp - 1 - STAGES;
+    const uint32_t cw = warp - kConsumer0;
     const uint32_t c = cw * 32 + lane;
     const uint64_t cover_lo = *sm.cover_lo(), cover_hi = *sm.cover_hi();
     int pending = -1;
     for (uint32_t k = 0;; ++k) {
-        const int s = int(k % STAGES);
-        const uint32_t par = (k / STAGES) & 1u;
-        const int w = warp_wait_or_end(sm.full(s), par, k, sm.end_iter());
-        if (w != 2 || !warp_wait(sm.carry_ready(s), par)) {
-            if (w != 1 && lane == 0) record_error(hdr, DWP_ERR_PIPELINE_TIMEOUT);
+        const int i = int(k % RING), o = int(k % SOUT);
+        const int w = warp_wait_or_end(sm.out_full(o), (k / SOUT) & 1u, k, sm.end_iter());
+        if (w != 2) {
+            if (w == 0 && lane == 0) record_error(hdr, DWP_ERR_PIPELINE_TIMEOUT);
             break;
         }
-        const uint32_t t = ld_volatile_smem(sm.tile_id(s));
+        const uint32_t t = ld_volatile_smem(sm.tile_id(i));
         if (t == kNoTile) break;
         uint32_t valid, bulk;
         tile_extent(t, valid, bulk);
@@ -398,22 +513,27 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         // a tile wholly inside [cover_lo, cover_hi) is stored in bulk; any
         // other tile row by row, only the covered rows
         const bool covered = base >= cover_lo && base + valid <= cover_hi;
-        if (ld_volatile_smem(sm.lbres(s)) != 0u || (!covered && (base >= cover_hi || base + valid <= cover_lo))) {
+        const bool outside = base >= cover_hi || base + valid <= cover_lo;
+        if (ld_volatile_smem(sm.lbres(i)) != 0u || outside) {
+            __syncwarp();
             if (lane == 0) {
+                mbar_arrive(sm.info_free(i));
                 bulk_wait_read<0>();
-                if (pending >= 0) mbar_arrive(sm.empty(pending));
-                mbar_arrive(sm.empty(s));
+                if (pending >= 0) mbar_arrive(sm.out_empty(pending));
+                mbar_arrive(sm.out_empty(o));
                 pending = -1;
             }
             __syncwarp();
             continue;
         }
-        uint32_t *buf = sm.data(s);
+        uint32_t *buf = sm.out_data(o);
         const uint32_t p0 = c * ITEMS;
-        const uint32_t hb = head_bits(sm.heads(s), p0, ITEMS);
-        const bool ph = sm.phead(s)[c] != 0;
-        const uint32_t pv = sm.prefix(s)[prefix_slot(c)];
-        uint32_t acc = ph ? pv : *sm.carry(s) + pv;
+        const uint32_t hb = head_bits(sm.heads(i), p0, ITEMS);
+        const bool phd = sm.phead(i)[c] != 0;
+        const uint32_t pv = sm.prefix(i)[prefix_slot(c)];
+        uint32_t acc = phd ? pv : *sm.carry(i) + pv;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sm.info_free(i));  // the info slot has been read
         if (valid == uint32_t(TILE) && covered) {
             uint4 *v4 = reinterpret_cast<uint4 *>(buf + p0);
 #pragma unroll
@@ -460,15 +580,15 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             const uint32_t w0 = cw * WE;
             const uint32_t w1 = covered ? min(w0 + uint32_t(WE), bulk) : w0;
             if (w1 > w0) {
-                bulk_store(out + base + w0, buf + w0, (w1 - w0) * 4u);
+                bulk_store_hint(out + base + w0, buf + w0, (w1 - w0) * 4u, l2_policy_evict_first());
                 bulk_commit();
                 bulk_wait_read<1>();
-                if (pending >= 0) mbar_arrive(sm.empty(pending));
-                pending = s;
+                if (pending >= 0) mbar_arrive(sm.out_empty(pending));
+                pending = o;
             } else {
                 bulk_wait_read<0>();
-                if (pending >= 0) mbar_arrive(sm.empty(pending));
-                mbar_arrive(sm.empty(s));
+                if (pending >= 0) mbar_arrive(sm.out_empty(pending));
+                mbar_arrive(sm.out_empty(o));
                 pending = -1;
             }
         }
