@@ -121,6 +121,9 @@ struct SegSmem {
     __device__ uint32_t *lbres(int i) const { return tile_id(i) + 3; }
     __device__ uint32_t *agg_head(int i) const { return tile_id(i) + 4; }
     __device__ uint32_t *first_head(int i) const { return tile_id(i) + 5; }
+    // tile holds at least one head; bitmap holds bits from an earlier use
+    __device__ uint32_t *has_heads(int i) const { return tile_id(i) + 6; }
+    __device__ uint32_t *heads_dirty(int i) const { return tile_id(i) + 7; }
     __device__ uint32_t *prefix(int i) const { return tile_id(i) + 8; }
     __device__ unsigned char *phead(int i) const {
         return reinterpret_cast<unsigned char *>(prefix(i) + C::kPrefixWords);
@@ -219,6 +222,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             mbar_init(sm.info_ready(i), 1);
             mbar_init(sm.carry_ready(i), 1);
             mbar_init(sm.info_free(i), NW);
+            *sm.heads_dirty(i) = 1u;  // bitmaps start uninitialised
         }
         *sm.abort_flag() = 0;
         *sm.end_iter() = kNoTile;
@@ -305,7 +309,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             uint32_t *heads = sm.heads(i);
 
             // -- S1: heads of this tile ------------------------------------
-            for (int q = int(lane); q < C::kHeadWords; q += 32) heads[q] = 0u;
+            // (the bitmap is cleared only if an earlier use of the slot set bits)
+            if (*sm.heads_dirty(i)) {
+                for (int q = int(lane); q < C::kHeadWords; q += 32) heads[q] = 0u;
+            }
             __syncwarp();
             const uint32_t *smp = sm.sample();
             uint32_t a = 0, b = nsample;  // first sample >= base
@@ -323,6 +330,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 const uint32_t hi = uint32_t(min(uint64_t(a) * stride, uint64_t(nseg) + 1));
                 k0 = warp_lower_bound(off, lo, hi, uint32_t(base), lane);
             }
+            uint32_t my_marks = 0;
             for (uint32_t kk = k0; kk <= nseg; kk += 32) {
                 const uint64_t idx = uint64_t(kk) + lane;
                 uint32_t p = 0xffffffffu;
@@ -330,9 +338,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 if (idx <= nseg && uint64_t(p) >= base && uint64_t(p) < tend) {
                     const uint32_t r = uint32_t(uint64_t(p) - base);
                     atomicOr(&heads[r >> 5], 1u << (r & 31u));
+                    ++my_marks;
                 }
                 if (__any_sync(0xffffffffu, idx > nseg || uint64_t(p) >= tend)) break;
             }
+            const bool tile_heads = __reduce_add_sync(0xffffffffu, my_marks) != 0u;
             __syncwarp();
 
             // -- per-thread (head, value) totals ---------------------------
@@ -342,9 +352,16 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 #pragma unroll
             for (int w2 = 0; w2 < NW; ++w2) {
                 const uint32_t c = lane + 32u * w2;
-                const uint32_t hb = head_bits(heads, c * ITEMS, ITEMS);
+                const uint32_t hb = tile_heads ? head_bits(heads, c * ITEMS, ITEMS) : 0u;
                 uint32_t acc = 0;
-                if (valid == uint32_t(TILE)) {
+                if (valid == uint32_t(TILE) && !hb) {
+                    const uint4 *v4 = reinterpret_cast<const uint4 *>(buf);
+#pragma unroll
+                    for (int v = 0; v < ITEMS / 4; ++v) {
+                        const uint4 q = v4[c * (ITEMS / 4) + v];
+                        acc += (q.x + q.y) + (q.z + q.w);
+                    }
+                } else if (valid == uint32_t(TILE)) {
                     const uint4 *v4 = reinterpret_cast<const uint4 *>(buf);
                     // only the items from the last head on count
                     const int from = hb ? 31 - __clz(hb) : 0;
@@ -363,7 +380,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                     }
                 }
                 pre[prefix_slot(c)] = acc;
-                ph[c] = hb ? 1 : 0;
+                if (tile_heads) ph[c] = hb ? 1 : 0;
             }
             // the input stage is no longer needed
             __syncwarp();
@@ -376,24 +393,33 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 const uint32_t c = lane * PER + j;
                 mv[j] = rv;
                 if (rh) mh |= 1u << j;
-                const uint32_t hv = ph[c];
+                const uint32_t hv = tile_heads ? ph[c] : 0u;
                 const uint32_t v = pre[prefix_slot(c)];
                 rv = hv ? v : rv + v;
                 rh |= hv;
             }
             sm.lane_tot(i)[lane] = rv;
-            sm.lane_head(i)[lane] = rh;
+            if (tile_heads) sm.lane_head(i)[lane] = rh;
             __syncwarp();
             uint32_t ev = 0, eh = 0, av = 0, ah = 0;  // lane exclusive pair, tile aggregate
+            if (tile_heads) {
 #pragma unroll
-            for (int l = 0; l < 32; ++l) {
-                const uint32_t v = sm.lane_tot(i)[l], h = sm.lane_head(i)[l];
-                if (uint32_t(l) < lane) {
-                    ev = h ? v : ev + v;
-                    eh |= h;
+                for (int l = 0; l < 32; ++l) {
+                    const uint32_t v = sm.lane_tot(i)[l], h = sm.lane_head(i)[l];
+                    if (uint32_t(l) < lane) {
+                        ev = h ? v : ev + v;
+                        eh |= h;
+                    }
+                    av = h ? v : av + v;
+                    ah |= h;
                 }
-                av = h ? v : av + v;
-                ah |= h;
+            } else {
+#pragma unroll
+                for (int l = 0; l < 32; ++l) {
+                    const uint32_t v = sm.lane_tot(i)[l];
+                    if (uint32_t(l) < lane) ev += v;
+                    av += v;
+                }
             }
             // each thread's exclusive pair: value in pre, head flag in ph
             // (lane l rewrites only its own PER slots)
@@ -401,14 +427,16 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             for (int j = 0; j < PER; ++j) {
                 const uint32_t hj = (mh >> j) & 1u;
                 pre[prefix_slot(lane * PER + j)] = hj ? mv[j] : ev + mv[j];
-                ph[lane * PER + j] = (hj | eh) ? 1 : 0;
+                if (tile_heads) ph[lane * PER + j] = (hj | eh) ? 1 : 0;
             }
             if (lane == 0) {
                 if (t != fault.never_publish_tile)
                     st_relaxed_gpu(desc + t, make_desc((t == 0 || ah) ? kPrefix : kAggregate, av));
                 *sm.agg(i) = av;
                 *sm.agg_head(i) = ah;
-                *sm.first_head(i) = heads[0] & 1u;
+                *sm.first_head(i) = tile_heads ? (heads[0] & 1u) : 0u;
+                *sm.has_heads(i) = tile_heads ? 1u : 0u;
+                *sm.heads_dirty(i) = tile_heads ? 1u : 0u;
                 *sm.lbres(i) = 0u;
             }
             __syncwarp();
@@ -528,8 +556,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         }
         uint32_t *buf = sm.out_data(o);
         const uint32_t p0 = c * ITEMS;
-        const uint32_t hb = head_bits(sm.heads(i), p0, ITEMS);
-        const bool phd = sm.phead(i)[c] != 0;
+        const bool th = *sm.has_heads(i) != 0u;
+        const uint32_t hb = th ? head_bits(sm.heads(i), p0, ITEMS) : 0u;
+        const bool phd = th && sm.phead(i)[c] != 0;
         const uint32_t pv = sm.prefix(i)[prefix_slot(c)];
         uint32_t acc = phd ? pv : *sm.carry(i) + pv;
         __syncwarp();
