@@ -69,7 +69,7 @@ struct SegConfig {
     static constexpr size_t kInfoBytes =
         64 + 4 * (kPrefixWords + kPHeadWords + kHeadWords + 33 + 33 + 33);
     static_assert(kInfoBytes % 8 == 0, "info slots hold mbarriers");
-    static constexpr size_t kBarBytes = 16 * (SIN_ + SOUT_);
+    static constexpr size_t kBarBytes = 16 * (SIN_ + SOUT_) + 8 * SIN_;
     // + abort, end, cover lo, cover hi, then the offset sample
     static constexpr size_t kSmemBytes = kStageBytes * (SIN_ + SOUT_) + kInfoBytes * RING_ +
                                          kBarBytes + 16 + 4 * kSample;
@@ -140,8 +140,10 @@ struct SegSmem {
     __device__ uint64_t *in_empty(int s) const { return bars() + C::kIn + s; }
     __device__ uint64_t *out_full(int o) const { return bars() + 2 * C::kIn + o; }
     __device__ uint64_t *out_empty(int o) const { return bars() + 2 * C::kIn + C::kOut + o; }
+    // the producer has written the tile id of input stage s (before its load)
+    __device__ uint64_t *id_ready(int s) const { return bars() + 2 * (C::kIn + C::kOut) + s; }
     __device__ uint32_t *words() const {
-        return reinterpret_cast<uint32_t *>(bars() + 2 * (C::kIn + C::kOut));
+        return reinterpret_cast<uint32_t *>(bars() + 2 * (C::kIn + C::kOut) + C::kIn);
     }
     __device__ uint32_t *abort_flag() const { return words(); }
     __device__ uint32_t *end_iter() const { return words() + 1; }
@@ -213,6 +215,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         for (int s = 0; s < SIN; ++s) {
             mbar_init(sm.in_full(s), 1);
             mbar_init(sm.in_empty(s), 1);
+            mbar_init(sm.id_ready(s), 1);
         }
         for (int o = 0; o < SOUT; ++o) {
             mbar_init(sm.out_full(o), 1);
@@ -259,6 +262,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 if (t >= num_tiles) t = kNoTile;
             }
             *reinterpret_cast<volatile uint32_t *>(sm.tile_id(i)) = t;
+            mbar_arrive(sm.id_ready(s));  // heads can be marked while the data is in flight
             if (t == kNoTile) {
                 stop_at(k);
                 mbar_arrive(sm.in_full(s));
@@ -282,7 +286,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         for (uint32_t use = 0;; ++use) {
             const uint32_t k = use * SIN + uint32_t(s);
             const int i = int(k % RING);
-            const int w = warp_wait_or_end(sm.in_full(s), use & 1u, k, sm.end_iter());
+            const int w = warp_wait_or_end(sm.id_ready(s), use & 1u, k, sm.end_iter());
             if (w != 2) {
                 if (w == 0 && lane == 0) record_error(hdr, DWP_ERR_PIPELINE_TIMEOUT);
                 return;
@@ -293,6 +297,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 return;
             }
             if (ld_volatile_smem(sm.abort_flag()) != 0) {
+                // the load may still be writing the stage: wait for it first
+                if (!warp_wait(sm.in_full(s), use & 1u) && lane == 0)
+                    record_error(hdr, DWP_ERR_PIPELINE_TIMEOUT);
                 if (lane == 0) {
                     st_relaxed_gpu(desc + t, make_desc(kPoison, 0u));
                     *sm.lbres(i) = 1u;
@@ -345,6 +352,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             const bool tile_heads = __reduce_add_sync(0xffffffffu, my_marks) != 0u;
             __syncwarp();
 
+            if (!warp_wait(sm.in_full(s), use & 1u)) {
+                // the producer always completes the load it announced
+                if (lane == 0) record_error(hdr, DWP_ERR_PIPELINE_TIMEOUT);
+                return;
+            }
             // -- per-thread (head, value) totals ---------------------------
             const uint32_t *buf = sm.in_data(s);
             uint32_t *pre = sm.prefix(i);
