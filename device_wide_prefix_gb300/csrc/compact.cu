@@ -7,19 +7,26 @@
 // flags is each kept record's output slot, so kept records keep their order
 // and never share a slot; the output length is the flag total.
 //
-// The pipeline is the plain scan's (scan.cu), over counts:
-//   producer warp   per tile, one bulk copy of the records and one of the
-//                   flag bytes, completing on the same mbarrier;
-//   tile warps      per tile: each consumer thread's kept count, their
-//                   exclusive prefix, the tile count published as the
-//                   aggregate, a u32-add look-back for the number of records
-//                   kept before the tile, the tile's inclusive count
-//                   published; the last tile writes the total to *count;
-//   consumer warps  thread c owns IT contiguous records.  Each warp reads
-//                   its records into registers, writes its kept ones to the
-//                   front of its own chunk of the stage buffer, in input
-//                   order, and streams that block to its output slots with
-//                   one bulk store.
+// The look-back needs only the flags (1 byte per 16-byte record), so the
+// records stay out of shared memory until their output slots are known:
+//   producer warp   takes a tile index from the atomic counter, loads the
+//                   tile's flag bytes with one bulk copy into the tile's
+//                   info slot, and asks L2 to prefetch the tile's records
+//                   (bulk prefetch, evict-last);
+//   tile warps      TW of them, iteration k taken by warp k % TW: each
+//                   consumer thread's kept count and their exclusive prefix,
+//                   the tile count published as the aggregate, a u32-add
+//                   look-back for the number of records kept before the
+//                   tile, the tile's inclusive count published; the last
+//                   tile writes the total to *count;
+//   loader warp     once a tile's output offset is known, loads its records
+//                   (now in L2) with one bulk copy into a ring of SOUT
+//                   output stages;
+//   consumer warps  thread c owns IT contiguous records.  Each warp reads its
+//                   records into registers, writes its kept ones to the front
+//                   of its own chunk of the stage, in input order, and
+//                   streams that block to its output slots with one bulk
+//                   store.
 // IT is odd, so 16-byte record reads at a thread stride of 16*IT bytes are
 // free of bank conflicts.
 #include <cuda_runtime.h>
@@ -31,28 +38,33 @@ namespace dwp {
 
 namespace {
 
-template <int NW_, int IT_, int STAGES_, int LOOKK_>
+template <int NW_, int IT_, int SOUT_, int RING_, int TW_, int LOOKK_>
 struct CompactConfig {
     static constexpr int kWarps = NW_;
     static constexpr int kItems = IT_;  // records per consumer thread
-    static constexpr int kStages = STAGES_;
+    static constexpr int kOut = SOUT_;
+    static constexpr int kRing = RING_;
+    static constexpr int kTileWarps = TW_;
     static constexpr int kLookK = LOOKK_;
-    static constexpr int kThreads = (1 + STAGES_ + NW_) * 32;
+    static constexpr int kThreads = (2 + TW_ + NW_) * 32;
     static constexpr int kConsumers = NW_ * 32;
     static constexpr int kWarpRecs = 32 * IT_;
     static constexpr int kTile = NW_ * 32 * IT_;  // records per tile
     static_assert(IT_ % 2 == 1, "IT must be odd");
     static_assert(kTile % 16 == 0, "flag bytes of a tile must start 16-byte aligned");
     static_assert(NW_ >= 1 && NW_ <= 32, "");
+    static_assert(RING_ % TW_ == 0, "a tile warp must own every use of its info slots");
+    static_assert(SOUT_ >= 2, "the loader waits for the output stage of iteration k - SOUT");
     static constexpr size_t kRecBytes = size_t(kTile) * 16;
-    static constexpr size_t kFlagBytes = (size_t(kTile) + 127) / 128 * 128;
-    static constexpr size_t kStageBytes = kRecBytes + kFlagBytes;
+    static constexpr size_t kFlagBytes = (size_t(kTile) + 15) / 16 * 16;
     static constexpr int kPrefixWords = kConsumers + kConsumers / 8;
-    // mbarriers 32 B; tile id, carry, look-back result, tile count 16 B;
-    // prefixes; lane totals 33; look-back scratch 33
-    static constexpr size_t kStageMeta = 48 + 4 * (kPrefixWords + 33 + 33);
-    static constexpr size_t kSmemBytes = (kStageBytes + kStageMeta) * kStages + 16;
-    static_assert(kStageBytes % 128 == 0, "stage buffers stay 128-byte aligned");
+    // info slot: 3 mbarriers + pad (32 B); tile id, carry, look-back result,
+    // tile count (16 B); flags; thread prefixes; lane totals 33; look-back
+    // scratch 33 (+ pad to 16 B)
+    static constexpr size_t kInfoBytes =
+        (48 + kFlagBytes + 4 * (kPrefixWords + 33 + 33) + 15) / 16 * 16;
+    static constexpr size_t kBarBytes = 16 * SOUT_;
+    static constexpr size_t kSmemBytes = kRecBytes * SOUT_ + kInfoBytes * RING_ + kBarBytes + 16;
 };
 
 #ifndef DWP_CMP_WARPS
@@ -61,47 +73,69 @@ struct CompactConfig {
 #ifndef DWP_CMP_ITEMS
 #define DWP_CMP_ITEMS 5
 #endif
-#ifndef DWP_CMP_STAGES
-#define DWP_CMP_STAGES 4
+#ifndef DWP_CMP_OUT
+#define DWP_CMP_OUT 4
 #endif
-using CmpCfg = CompactConfig<DWP_CMP_WARPS, DWP_CMP_ITEMS, DWP_CMP_STAGES, 4>;
+#ifndef DWP_CMP_RING
+#define DWP_CMP_RING 12
+#endif
+#ifndef DWP_CMP_TILEWARPS
+#define DWP_CMP_TILEWARPS 12
+#endif
+#ifndef DWP_CMP_LOOKK
+#define DWP_CMP_LOOKK 1
+#endif
+using CmpCfg = CompactConfig<DWP_CMP_WARPS, DWP_CMP_ITEMS, DWP_CMP_OUT, DWP_CMP_RING,
+                             DWP_CMP_TILEWARPS, DWP_CMP_LOOKK>;
 
 template <class C>
 struct CmpSmem {
     unsigned char *base;
     __device__ explicit CmpSmem(unsigned char *p) : base(p) {}
-    __device__ uint4 *recs(int s) const {
-        return reinterpret_cast<uint4 *>(base + size_t(s) * C::kStageBytes);
+    __device__ uint4 *recs(int o) const {
+        return reinterpret_cast<uint4 *>(base + size_t(o) * C::kRecBytes);
     }
-    __device__ unsigned char *flags(int s) const {
-        return base + size_t(s) * C::kStageBytes + C::kRecBytes;
+    __device__ unsigned char *info(int i) const {
+        return base + C::kRecBytes * C::kOut + size_t(i) * C::kInfoBytes;
     }
-    __device__ unsigned char *meta(int s) const {
-        return base + C::kStageBytes * C::kStages + size_t(s) * C::kStageMeta;
+    __device__ uint64_t *flags_full(int i) const { return reinterpret_cast<uint64_t *>(info(i)); }
+    __device__ uint64_t *carry_ready(int i) const { return flags_full(i) + 1; }
+    __device__ uint64_t *info_free(int i) const { return flags_full(i) + 2; }
+    __device__ uint32_t *tile_id(int i) const { return reinterpret_cast<uint32_t *>(info(i) + 32); }
+    __device__ uint32_t *carry(int i) const { return tile_id(i) + 1; }
+    __device__ uint32_t *lbres(int i) const { return tile_id(i) + 2; }
+    __device__ uint32_t *tile_count(int i) const { return tile_id(i) + 3; }
+    __device__ unsigned char *flags(int i) const { return info(i) + 48; }
+    __device__ uint32_t *prefix(int i) const {
+        return reinterpret_cast<uint32_t *>(flags(i) + C::kFlagBytes);
     }
-    __device__ uint64_t *full(int s) const { return reinterpret_cast<uint64_t *>(meta(s)); }
-    __device__ uint64_t *carry_ready(int s) const { return full(s) + 1; }
-    __device__ uint64_t *empty(int s) const { return full(s) + 2; }
-    __device__ uint32_t *tile_id(int s) const { return reinterpret_cast<uint32_t *>(meta(s) + 32); }
-    __device__ uint32_t *carry(int s) const { return tile_id(s) + 1; }
-    __device__ uint32_t *lbres(int s) const { return tile_id(s) + 2; }
-    __device__ uint32_t *tile_count(int s) const { return tile_id(s) + 3; }
-    __device__ uint32_t *prefix(int s) const { return tile_id(s) + 4; }
-    __device__ uint32_t *lane_tot(int s) const { return prefix(s) + C::kPrefixWords; }
-    __device__ uint32_t *lb_scratch(int s) const { return lane_tot(s) + 33; }
+    __device__ uint32_t *lane_tot(int i) const { return prefix(i) + C::kPrefixWords; }
+    __device__ uint32_t *lb_scratch(int i) const { return lane_tot(i) + 33; }
+    __device__ uint64_t *bars() const {
+        return reinterpret_cast<uint64_t *>(base + C::kRecBytes * C::kOut + C::kInfoBytes * C::kRing);
+    }
+    __device__ uint64_t *out_full(int o) const { return bars() + o; }
+    __device__ uint64_t *out_empty(int o) const { return bars() + C::kOut + o; }
     __device__ uint32_t *abort_flag() const {
-        return reinterpret_cast<uint32_t *>(base + (C::kStageBytes + C::kStageMeta) * C::kStages);
+        return reinterpret_cast<uint32_t *>(bars() + 2 * C::kOut);
     }
     __device__ uint32_t *end_iter() const { return abort_flag() + 1; }
 };
 
-// Keep flag of record pos of a tile: from the stage below `fbulk`, from
-// global memory below `valid`, else 0.
+// Keep flag of record pos of a tile: from the slot below `fbulk`, from global
+// memory below `valid`, else 0.
 __device__ __forceinline__ bool keep_at(const unsigned char *sflags, const uint8_t *gflags,
                                         uint64_t base, uint32_t pos, uint32_t fbulk, uint32_t valid) {
     if (pos < fbulk) return sflags[pos] != 0;
     if (pos < valid) return gflags[base + pos] != 0;
     return false;
+}
+
+// Ask L2 to fetch [src, src + bytes) ahead of use, with an eviction priority.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes, uint64_t policy) {
+    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(src),
+                 "r"(bytes), "l"(policy)
+                 : "memory");
 }
 
 template <class C>
@@ -110,18 +144,24 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                    uint32_t *count, uint32_t num_tiles, ScratchHeader *hdr, uint64_t *desc,
                    FaultConfig fault) {
     using Op = OpU32Add;
-    constexpr int NW = C::kWarps, IT = C::kItems, STAGES = C::kStages, TILE = C::kTile;
+    constexpr int NW = C::kWarps, IT = C::kItems, TILE = C::kTile;
+    constexpr int SOUT = C::kOut, RING = C::kRing, TW = C::kTileWarps;
     constexpr int WR = C::kWarpRecs;
     constexpr uint32_t NCONS = C::kConsumers;
+    constexpr uint32_t kTileWarp0 = 1, kLoader = 1 + TW, kConsumer0 = 2 + TW;
 
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const CmpSmem<C> sm(smem_raw);
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(sm.full(s), 1);
-            mbar_init(sm.carry_ready(s), 1);
-            mbar_init(sm.empty(s), NW);
+        for (int o = 0; o < SOUT; ++o) {
+            mbar_init(sm.out_full(o), 1);
+            mbar_init(sm.out_empty(o), NW);
+        }
+        for (int i = 0; i < RING; ++i) {
+            mbar_init(sm.flags_full(i), 1);
+            mbar_init(sm.carry_ready(i), 1);
+            mbar_init(sm.info_free(i), NW);
         }
         *sm.abort_flag() = 0;
         *sm.end_iter() = kNoTile;
@@ -136,15 +176,18 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         valid = rem < uint64_t(TILE) ? uint32_t(rem) : uint32_t(TILE);
         fbulk = valid & ~15u;
     };
+    auto stop_at = [&](uint32_t k) { *reinterpret_cast<volatile uint32_t *>(sm.end_iter()) = k; };
 
     if (warp == 0) {
         // ------------------------------------------------------- producer
         if (lane != 0) return;
+        const uint64_t keep = l2_policy_evict_last();
         for (uint32_t k = 0;; ++k) {
-            const int s = int(k % STAGES);
-            if (k >= STAGES && !mbar_wait(sm.empty(s), ((k / STAGES) - 1) & 1u, kPipeWaitLimit)) {
+            const int i = int(k % RING);
+            if (k >= uint32_t(RING) &&
+                !mbar_wait(sm.info_free(i), ((k / RING) - 1) & 1u, kPipeWaitLimit)) {
                 record_error(hdr, DWP_ERR_PIPELINE_TIMEOUT);
-                *reinterpret_cast<volatile uint32_t *>(sm.end_iter()) = k - 1;
+                stop_at(k - 1);
                 return;
             }
             uint32_t t = kNoTile;
@@ -152,43 +195,47 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 t = atomicAdd(&hdr->tile_counter, 1u);
                 if (t >= num_tiles) t = kNoTile;
             }
-            *reinterpret_cast<volatile uint32_t *>(sm.tile_id(s)) = t;
+            *reinterpret_cast<volatile uint32_t *>(sm.tile_id(i)) = t;
             if (t == kNoTile) {
-                *reinterpret_cast<volatile uint32_t *>(sm.end_iter()) = k;
-                mbar_arrive(sm.full(s));
+                stop_at(k);
+                mbar_arrive(sm.flags_full(i));
                 return;
             }
             uint32_t valid, fbulk;
             tile_extent(t, valid, fbulk);
             const uint64_t base = uint64_t(t) * TILE;
-            mbar_arrive_expect_tx(sm.full(s), valid * 16u + fbulk);
-            bulk_load(sm.recs(s), recs + base, valid * 16u, sm.full(s));
-            if (fbulk) bulk_load(sm.flags(s), flags + base, fbulk, sm.full(s));
+            bulk_prefetch_l2(recs + base, valid * 16u, keep);
+            if (fbulk) {
+                mbar_arrive_expect_tx(sm.flags_full(i), fbulk);
+                bulk_load(sm.flags(i), flags + base, fbulk, sm.flags_full(i));
+            } else {
+                mbar_arrive(sm.flags_full(i));
+            }
         }
     }
 
-    if (warp <= uint32_t(STAGES)) {
+    if (warp >= kTileWarp0 && warp < kLoader) {
         // ----------------------------------------------------- tile warps
-        const int s = int(warp) - 1;
+        const uint32_t j = warp - kTileWarp0;
         bool draining = false;
-        for (uint32_t use = 0;; ++use) {
-            const int w = warp_wait_or_end(sm.full(s), use & 1u, use * STAGES + uint32_t(s),
-                                           sm.end_iter());
+        for (uint32_t k = j;; k += TW) {
+            const int i = int(k % RING);
+            const int w = warp_wait_or_end(sm.flags_full(i), (k / RING) & 1u, k, sm.end_iter());
             if (w != 2) {
                 if (w == 0 && lane == 0) record_error(hdr, DWP_ERR_PIPELINE_TIMEOUT);
                 return;
             }
-            const uint32_t t = ld_volatile_smem(sm.tile_id(s));
+            const uint32_t t = ld_volatile_smem(sm.tile_id(i));
             if (t == kNoTile) {
-                if (lane == 0) mbar_arrive(sm.carry_ready(s));
+                if (lane == 0) mbar_arrive(sm.carry_ready(i));
                 return;
             }
             if (!draining && ld_volatile_smem(sm.abort_flag()) != 0) draining = true;
             if (draining) {
                 if (lane == 0) {
                     st_relaxed_gpu(desc + t, make_desc(kPoison, 0u));
-                    *sm.lbres(s) = 1u;
-                    mbar_arrive(sm.carry_ready(s));
+                    *sm.lbres(i) = 1u;
+                    mbar_arrive(sm.carry_ready(i));
                 }
                 __syncwarp();
                 continue;
@@ -196,19 +243,19 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             uint32_t valid, fbulk;
             tile_extent(t, valid, fbulk);
             const uint64_t base = uint64_t(t) * TILE;
-            const unsigned char *sf = sm.flags(s);
-            uint32_t *pre = sm.prefix(s);
-            uint32_t *lt = sm.lane_tot(s);
+            const unsigned char *sf = sm.flags(i);
+            uint32_t *pre = sm.prefix(i);
+            uint32_t *lt = sm.lane_tot(i);
             // K1: kept count of consumer thread c = lane + 32w (records c*IT ..)
 #pragma unroll
-            for (int w = 0; w < NW; ++w) {
-                const uint32_t c = lane + 32u * w;
+            for (int w2 = 0; w2 < NW; ++w2) {
+                const uint32_t c = lane + 32u * w2;
                 uint32_t cnt = 0;
                 if (valid == uint32_t(TILE)) {
 #pragma unroll
-                    for (int j = 0; j < IT; ++j) cnt += sf[c * IT + j] != 0;
+                    for (int q = 0; q < IT; ++q) cnt += sf[c * IT + q] != 0;
                 } else {
-                    for (int j = 0; j < IT; ++j) cnt += keep_at(sf, flags, base, c * IT + j, fbulk, valid);
+                    for (int q = 0; q < IT; ++q) cnt += keep_at(sf, flags, base, c * IT + q, fbulk, valid);
                 }
                 pre[prefix_slot(c)] = cnt;
             }
@@ -217,9 +264,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             constexpr int PER = NCONS / 32;
             uint32_t mine[PER], run = 0;
 #pragma unroll
-            for (int j = 0; j < PER; ++j) {
-                mine[j] = run;
-                run += pre[prefix_slot(lane * PER + j)];
+            for (int q = 0; q < PER; ++q) {
+                mine[q] = run;
+                run += pre[prefix_slot(lane * PER + q)];
             }
             lt[lane] = run;
             __syncwarp();
@@ -231,12 +278,13 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 total += v;
             }
 #pragma unroll
-            for (int j = 0; j < PER; ++j) pre[prefix_slot(lane * PER + j)] = lane_excl + mine[j];
+            for (int q = 0; q < PER; ++q) pre[prefix_slot(lane * PER + q)] = lane_excl + mine[q];
             if (lane == 0 && t != fault.never_publish_tile)
                 st_relaxed_gpu(desc + t, make_desc(t == 0 ? kPrefix : kAggregate, total));
             uint32_t carry = 0;
             int rc = 0;
-            if (t != 0) rc = lookback<Op, C::kLookK>(desc, t, lane, fault.spin_limit, sm.lb_scratch(s), &carry);
+            if (t != 0)
+                rc = lookback<Op, C::kLookK>(desc, t, lane, fault.spin_limit, sm.lb_scratch(i), &carry);
             if (lane == 0) {
                 if (rc == 0) {
                     if (t != 0 && t != fault.never_publish_tile)
@@ -247,71 +295,107 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                     if (rc == 2) record_error(hdr, DWP_ERR_LOOKBACK_TIMEOUT);
                     *reinterpret_cast<volatile uint32_t *>(sm.abort_flag()) = 1u;
                 }
-                *sm.carry(s) = carry;
-                *sm.tile_count(s) = total;
-                *sm.lbres(s) = uint32_t(rc);
+                *sm.carry(i) = carry;
+                *sm.tile_count(i) = total;
+                *sm.lbres(i) = uint32_t(rc);
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(sm.carry_ready(s));
+            if (lane == 0) mbar_arrive(sm.carry_ready(i));
             if (rc != 0) draining = true;
         }
     }
 
+    if (warp == kLoader) {
+        // ------------------------------------------------------------ loader
+        if (lane != 0) return;
+        const uint64_t drop = l2_policy_evict_first();
+        for (uint32_t k = 0;; ++k) {
+            const int i = int(k % RING), o = int(k % SOUT);
+            int w = 0;
+            for (uint32_t p = 0; p < kPipeWaitLimit; ++p) {
+                if (mbar_try_wait(sm.carry_ready(i), (k / RING) & 1u)) { w = 2; break; }
+                if (ld_volatile_smem(sm.end_iter()) < k) { w = 1; break; }
+                if (p >= 8) __nanosleep(64);
+            }
+            if (w == 2 && k >= uint32_t(SOUT) &&
+                !mbar_wait(sm.out_empty(o), ((k / SOUT) - 1) & 1u, kPipeWaitLimit))
+                w = 0;
+            if (w != 2) {
+                if (w == 0) record_error(hdr, DWP_ERR_PIPELINE_TIMEOUT);
+                return;
+            }
+            const uint32_t t = ld_volatile_smem(sm.tile_id(i));
+            if (t == kNoTile || ld_volatile_smem(sm.lbres(i)) != 0u ||
+                ld_volatile_smem(sm.tile_count(i)) == 0u) {
+                // nothing to load: sentinel, poisoned tile, or no record kept
+                mbar_arrive(sm.out_full(o));
+                if (t == kNoTile) return;
+                continue;
+            }
+            uint32_t valid, fbulk;
+            tile_extent(t, valid, fbulk);
+            mbar_arrive_expect_tx(sm.out_full(o), valid * 16u);
+            bulk_load_hint(sm.recs(o), recs + uint64_t(t) * TILE, valid * 16u, sm.out_full(o), drop);
+        }
+    }
+
+    if (warp < kConsumer0) return;
     // ---------------------------------------------------------- consumers
-    const uint32_t cw = warp - 1 - STAGES;
+    const uint32_t cw = warp - kConsumer0;
     const uint32_t c = cw * 32 + lane;
+    const uint64_t drop = l2_policy_evict_first();
     int pending = -1;
     for (uint32_t k = 0;; ++k) {
-        const int s = int(k % STAGES);
-        const uint32_t par = (k / STAGES) & 1u;
-        const int w = warp_wait_or_end(sm.full(s), par, k, sm.end_iter());
-        if (w != 2 || !warp_wait(sm.carry_ready(s), par)) {
-            if (w != 1 && lane == 0) record_error(hdr, DWP_ERR_PIPELINE_TIMEOUT);
+        const int i = int(k % RING), o = int(k % SOUT);
+        const int w = warp_wait_or_end(sm.out_full(o), (k / SOUT) & 1u, k, sm.end_iter());
+        if (w != 2) {
+            if (w == 0 && lane == 0) record_error(hdr, DWP_ERR_PIPELINE_TIMEOUT);
             break;
         }
-        const uint32_t t = ld_volatile_smem(sm.tile_id(s));
+        const uint32_t t = ld_volatile_smem(sm.tile_id(i));
         if (t == kNoTile) break;
         uint32_t nkeep = 0, first = 0;  // this warp's kept records and its first output slot
-        if (ld_volatile_smem(sm.lbres(s)) == 0u) {
+        if (ld_volatile_smem(sm.lbres(i)) == 0u && *sm.tile_count(i) != 0u) {
             uint32_t valid, fbulk;
             tile_extent(t, valid, fbulk);
             const uint64_t base = uint64_t(t) * TILE;
-            uint4 *region = sm.recs(s) + cw * WR;
-            const uint32_t *pre = sm.prefix(s);
+            uint4 *region = sm.recs(o) + cw * WR;
+            const uint32_t *pre = sm.prefix(i);
             const uint32_t wfirst = pre[prefix_slot(cw * 32)];
             const uint32_t wend =
-                cw + 1 < uint32_t(NW) ? pre[prefix_slot(cw * 32 + 32)] : *sm.tile_count(s);
+                cw + 1 < uint32_t(NW) ? pre[prefix_slot(cw * 32 + 32)] : *sm.tile_count(i);
             nkeep = wend - wfirst;
-            first = *sm.carry(s) + wfirst;
+            first = *sm.carry(i) + wfirst;
             // K3: read this thread's records, then (after the whole warp has
             // read) write the kept ones to their in-warp slots, in order
             uint4 r[IT];
             uint32_t keepm = 0;
 #pragma unroll
-            for (int j = 0; j < IT; ++j) {
-                const uint32_t pos = c * IT + j;
-                if (pos < valid) r[j] = sm.recs(s)[pos];
-                if (keep_at(sm.flags(s), flags, base, pos, fbulk, valid)) keepm |= 1u << j;
+            for (int q = 0; q < IT; ++q) {
+                const uint32_t pos = c * IT + q;
+                if (pos < valid) r[q] = sm.recs(o)[pos];
+                if (keep_at(sm.flags(i), flags, base, pos, fbulk, valid)) keepm |= 1u << q;
             }
-            __syncwarp();
             uint32_t slot = pre[prefix_slot(c)] - wfirst;
+            __syncwarp();
 #pragma unroll
-            for (int j = 0; j < IT; ++j)
-                if ((keepm >> j) & 1u) region[slot++] = r[j];
+            for (int q = 0; q < IT; ++q)
+                if ((keepm >> q) & 1u) region[slot++] = r[q];
             fence_proxy_async_smem();
         }
         __syncwarp();
         if (lane == 0) {
+            mbar_arrive(sm.info_free(i));  // flags and prefixes have been read
             if (nkeep) {
-                bulk_store(out + first, sm.recs(s) + cw * WR, nkeep * 16u);
+                bulk_store_hint(out + first, sm.recs(o) + cw * WR, nkeep * 16u, drop);
                 bulk_commit();
                 bulk_wait_read<1>();
-                if (pending >= 0) mbar_arrive(sm.empty(pending));
-                pending = s;
+                if (pending >= 0) mbar_arrive(sm.out_empty(pending));
+                pending = o;
             } else {
                 bulk_wait_read<0>();
-                if (pending >= 0) mbar_arrive(sm.empty(pending));
-                mbar_arrive(sm.empty(s));
+                if (pending >= 0) mbar_arrive(sm.out_empty(pending));
+                mbar_arrive(sm.out_empty(o));
                 pending = -1;
             }
         }
