@@ -92,7 +92,7 @@ struct ScanConfig {
 #define DWP_SCAN_RING 16
 #endif
 #ifndef DWP_SCAN_LOOKERS
-#define DWP_SCAN_LOOKERS 8
+#define DWP_SCAN_LOOKERS 16
 #endif
 #ifndef DWP_SCAN_LOOKK
 #define DWP_SCAN_LOOKK 1

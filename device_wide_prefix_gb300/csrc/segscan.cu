@@ -91,7 +91,7 @@ struct SegConfig {
 #define DWP_SEG_RING 12
 #endif
 #ifndef DWP_SEG_LOOKERS
-#define DWP_SEG_LOOKERS 6
+#define DWP_SEG_LOOKERS 12
 #endif
 #ifndef DWP_SEG_LOOKK
 #define DWP_SEG_LOOKK 1
