@@ -200,6 +200,9 @@ def main() -> None:
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=10.0)
+    ap.add_argument("--only", default=None, choices=["segscan", "compact"],
+                    help="time only this workload (at --log2n) and print its entry; for "
+                         "profiler captures")
     ap.add_argument("--log2n", type=int, default=28,
                     help="problem size 2^k (default 28, the benchmarked workload; smaller "
                          "sizes are for profiler captures)")
@@ -213,6 +216,9 @@ def main() -> None:
 
     if args.impl == "reference":
         run_reference(args, rank)
+        return
+    if args.only:
+        run_only(args)
         return
 
     import torch
@@ -404,12 +410,25 @@ def measure_secondary(dwp, lib, dev, stream, peaks, x, y, scratch, need) -> dict
     return out
 
 
-def measure_compact(dwp, lib, dev, stream, peaks) -> dict:
+def run_only(args) -> None:
+    """One workload alone, `args.steps` timed calls, for profiler captures."""
+    import torch
+    import device_wide_prefix_gb300 as dwp
+    dev = torch.device("cuda", 0)
+    lib = dwp.load()
+    stream = torch.cuda.current_stream(dev)
+    fn = measure_segscan if args.only == "segscan" else measure_compact
+    r = fn(dwp, lib, dev, stream, measured_peaks(), log2n=args.log2n, steps=args.steps,
+           warmup=args.warmup)
+    print(json.dumps({"only": args.only, **r}), flush=True)
+
+
+def measure_compact(dwp, lib, dev, stream, peaks, log2n=26, steps=100, warmup=5) -> dict:
     """Stable compaction of 2^26 16-byte records {u32 id, 3 x f32 N(0,1)} by
     Bernoulli(0.3) byte flags."""
     import ctypes
     import torch
-    n = 1 << 26
+    n = 1 << log2n
     rec = torch.from_numpy(synth.records(n).view(np.int32)).to(dev)
     flags = torch.from_numpy(synth.keep_flags(n)).to(dev)
     out = torch.empty_like(rec)
@@ -421,7 +440,7 @@ def measure_compact(dwp, lib, dev, stream, peaks) -> dict:
             ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(cnt.data_ptr()),
             ctypes.c_void_p(scratch.data_ptr()), ctypes.byref(sb),
             ctypes.c_void_p(int(stream.cuda_stream)))
-    ms = time_calls(lambda: lib.dwp_compact_by_flags(*args), 100, 5, stream)
+    ms = time_calls(lambda: lib.dwp_compact_by_flags(*args), steps, warmup, stream)
     if dwp.read_status(scratch) != dwp.DWP_SUCCESS:
         raise RuntimeError("compaction reported a device-side error")
     k = int(cnt.item())
@@ -429,16 +448,16 @@ def measure_compact(dwp, lib, dev, stream, peaks) -> dict:
     gbs = alg / (ms * 1e-3) / 1e9
     return {"n": n, "kept": k, "ms": ms, "Gelem_s": n / (ms * 1e-3) / 1e9, "GB_s": gbs,
             "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": alg,
-            "workload": "stable compaction of 2^26 16-byte records, keep flag Bernoulli(0.3) "
-                        "(SplitMix64 seed 0xD3B00004)"}
+            "workload": "stable compaction of 2^%d 16-byte records, keep flag Bernoulli(0.3) "
+                        "(SplitMix64 seed 0xD3B00004)" % log2n}
 
 
-def measure_segscan(dwp, lib, dev, stream, peaks) -> dict:
+def measure_segscan(dwp, lib, dev, stream, peaks, log2n=27, steps=200, warmup=5) -> dict:
     """Segmented exclusive u32 scan, n = 2^27 values in [0, 255], Zipf(1.2)
     segment lengths capped at 2^22 with 5% empty segments (CSR offsets)."""
     import ctypes
     import torch
-    n = 1 << 27
+    n = 1 << log2n
     off_np = synth.segment_offsets(n)
     nseg = off_np.size - 1
     v = torch.from_numpy(synth.u32_byte_values(n).view(np.int32)).to(dev)
@@ -450,14 +469,14 @@ def measure_segscan(dwp, lib, dev, stream, peaks) -> dict:
     args = (ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(off.data_ptr()), nseg,
             ctypes.c_void_p(y.data_ptr()), n, dwp.DWP_EXCLUSIVE, ctypes.c_void_p(scratch.data_ptr()),
             ctypes.byref(sb), ctypes.c_void_p(int(stream.cuda_stream)))
-    ms = time_calls(lambda: lib.dwp_segmented_scan_u32(*args), 200, 5, stream)
+    ms = time_calls(lambda: lib.dwp_segmented_scan_u32(*args), steps, warmup, stream)
     if dwp.read_status(scratch) != dwp.DWP_SUCCESS:
         raise RuntimeError("segmented scan reported a device-side error")
     alg = 8 * n + 4 * (nseg + 1)
     gbs = alg / (ms * 1e-3) / 1e9
     return {"n": n, "segments": nseg, "ms": ms, "Gelem_s": n / (ms * 1e-3) / 1e9, "GB_s": gbs,
             "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": alg,
-            "workload": "segmented exclusive u32 sum scan, n=2^27 values in [0,255], Zipf(1.2) "
+            "workload": ("segmented exclusive u32 sum scan, n=2^%d values in [0,255], Zipf(1.2) " % log2n) +
                         "lengths capped at 2^22, 5% empty, CSR offsets (SplitMix64 seed 0xD3B00005)"}
 
 
