@@ -131,13 +131,6 @@ __device__ __forceinline__ bool keep_at(const unsigned char *sflags, const uint8
     return false;
 }
 
-// Ask L2 to fetch [src, src + bytes) ahead of use, with an eviction priority.
-__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes, uint64_t policy) {
-    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(src),
-                 "r"(bytes), "l"(policy)
-                 : "memory");
-}
-
 template <class C>
 __global__ void __launch_bounds__(C::kThreads, 1)
     compact_kernel(const uint4 *recs, const uint8_t *flags, uint64_t n, uint4 *out,

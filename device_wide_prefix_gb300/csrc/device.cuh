@@ -140,6 +140,13 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
 }
 
 // bulk_load with an L2 eviction-priority policy for the lines it reads.
+// Ask L2 to fetch [src, src + bytes) ahead of use, with an eviction priority.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes, uint64_t policy) {
+    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(src),
+                 "r"(bytes), "l"(policy)
+                 : "memory");
+}
+
 __device__ __forceinline__ void bulk_load_hint(void *smem_dst, const void *gmem_src, uint32_t bytes,
                                                uint64_t *bar, uint64_t policy) {
     asm volatile(

@@ -6,7 +6,9 @@
 // strategies").  Per block:
 //
 //   producer warp    takes tile indices from the atomic counter in the order
-//                    tiles start and streams each tile global -> shared with
+//                    tiles start, AHEAD iterations before their load, and asks
+//                    L2 to prefetch each tile when it takes it; when an input
+//                    stage frees up it streams the tile global -> shared with
 //                    one bulk (TMA) copy into a ring of SIN input stages;
 //   reducer warps    one per input stage.  For its tile: every consumer
 //                    thread's total and their exclusive prefix (block
@@ -35,6 +37,15 @@
 // memory at full bandwidth; held in L2 they do not.  Shared memory now holds
 // a tile only while it is reduced and while it is scanned and stored.
 //
+// Why the prefetch: with the reload in place the producer spent over 90% of
+// its waiting time on a free input stage, because a bulk load straight from
+// HBM held its stage for about 3 us.  Prefetched into L2 two iterations
+// early, the load finds most of the tile there and the stage turns over
+// faster, so two input stages do the work of three and more.  The lead is
+// short on purpose: a tile whose index is taken early publishes its
+// aggregate later, and every later tile's look-back waits for it (leads of
+// 4 to 10 iterations were slower than no lead at all).
+//
 // ITEMS is an odd multiple of 4, so the 16-byte shared-memory accesses of a
 // quarter warp (thread stride 16*odd bytes) fall in 8 distinct bank groups.
 // No block-wide barrier is used after set-up: warps meet only at mbarriers,
@@ -46,7 +57,7 @@
 
 namespace dwp {
 
-template <int NW_, int ITEMS_, int SIN_, int SOUT_, int RING_, int LW_, int LOOKK_>
+template <int NW_, int ITEMS_, int SIN_, int SOUT_, int RING_, int LW_, int LOOKK_, int AHEAD_>
 struct ScanConfig {
     static constexpr int kWarps = NW_;       // consumer warps (one chunk of the tile each)
     static constexpr int kItems = ITEMS_;    // contiguous elements per consumer thread
@@ -55,6 +66,7 @@ struct ScanConfig {
     static constexpr int kRing = RING_;      // tile-info slots
     static constexpr int kLookers = LW_;     // look-back warps
     static constexpr int kLookK = LOOKK_;    // look-back sub-windows of 32 per poll
+    static constexpr int kAhead = AHEAD_;    // iterations a tile index is drawn before its load
     static constexpr int kThreads = (2 + SIN_ + LW_ + NW_) * 32;
     static constexpr int kConsumers = NW_ * 32;
     static constexpr int kWarpElems = 32 * ITEMS_;
@@ -63,17 +75,22 @@ struct ScanConfig {
     static_assert(NW_ >= 1 && NW_ <= 32, "one 32-slot row of thread totals per consumer warp");
     static_assert(RING_ % LW_ == 0, "a look-back warp must own every use of its info slots");
     static_assert(SOUT_ >= 2, "the reloader waits for the output stage of iteration k - SOUT");
-    static_assert(RING_ >= SIN_ + SOUT_ + 2, "info ring shorter than the work in flight");
+    static_assert(RING_ >= SIN_ + SOUT_ + 2 + AHEAD_, "info ring shorter than the work in flight");
     static constexpr size_t kStageBytes = size_t(kTile) * 4;
     static constexpr int kPrefixWords = kConsumers + kConsumers / 8;
     // info slot: 3 mbarriers + pad (32 B); tile id, aggregate, carry,
     // look-back result (16 B); thread prefixes; 33 lane totals; 33 words of
     // look-back scratch
-    static constexpr size_t kInfoBytes = 48 + 4 * (kPrefixWords + 33 + 33);
+    static constexpr size_t kInfoBytes = 48 + 4 * kPrefixWords;
+    // per-warp scratch after the barriers: 33 lane totals per reducer, 33
+    // words per look-back warp (f32 warp reduction)
+    static constexpr size_t kWarpScratchBytes = 4 * 33 * (SIN_ + LW_);
     // stage barriers: per input stage full + empty, per output stage ready + empty
     static constexpr size_t kBarBytes = 16 * (SIN_ + SOUT_);
     static constexpr size_t kSmemBytes =
-        kStageBytes * (SIN_ + SOUT_) + kInfoBytes * RING_ + kBarBytes + 16;
+        kStageBytes * (SIN_ + SOUT_) + kInfoBytes * RING_ + kBarBytes + 16 + kWarpScratchBytes;
+    static_assert(kThreads <= 1024, "more than 1024 threads per block");
+    static_assert(kSmemBytes <= 232448, "more than 227 KiB of shared memory per block");
 };
 
 #ifndef DWP_SCAN_WARPS
@@ -83,7 +100,7 @@ struct ScanConfig {
 #define DWP_SCAN_ITEMS 28
 #endif
 #ifndef DWP_SCAN_IN
-#define DWP_SCAN_IN 3
+#define DWP_SCAN_IN 2
 #endif
 #ifndef DWP_SCAN_OUT
 #define DWP_SCAN_OUT 4
@@ -97,8 +114,11 @@ struct ScanConfig {
 #ifndef DWP_SCAN_LOOKK
 #define DWP_SCAN_LOOKK 1
 #endif
+#ifndef DWP_SCAN_AHEAD
+#define DWP_SCAN_AHEAD 2
+#endif
 using ScanCfg = ScanConfig<DWP_SCAN_WARPS, DWP_SCAN_ITEMS, DWP_SCAN_IN, DWP_SCAN_OUT,
-                           DWP_SCAN_RING, DWP_SCAN_LOOKERS, DWP_SCAN_LOOKK>;
+                           DWP_SCAN_RING, DWP_SCAN_LOOKERS, DWP_SCAN_LOOKK, DWP_SCAN_AHEAD>;
 
 // Shared-memory layout of one block.
 template <class C>
@@ -122,8 +142,7 @@ struct ScanSmem {
     __device__ uint32_t *carry(int i) const { return tile_id(i) + 2; }
     __device__ uint32_t *lbres(int i) const { return tile_id(i) + 3; }
     __device__ uint32_t *prefix(int i) const { return tile_id(i) + 4; }
-    __device__ uint32_t *lane_tot(int i) const { return prefix(i) + C::kPrefixWords; }
-    __device__ uint32_t *lb_scratch(int i) const { return lane_tot(i) + 33; }
+
     __device__ uint64_t *bars() const {
         return reinterpret_cast<uint64_t *>(base + C::kStageBytes * (C::kIn + C::kOut) +
                                             C::kInfoBytes * C::kRing);
@@ -137,6 +156,9 @@ struct ScanSmem {
     }
     // first ring iteration that holds no tile (set once by the producer)
     __device__ uint32_t *end_iter() const { return abort_flag() + 1; }
+    // reducer r's 33 lane totals; look-back warp j's 33-word scratch
+    __device__ uint32_t *lane_tot(int r) const { return abort_flag() + 4 + 33 * r; }
+    __device__ uint32_t *lb_scratch(int j) const { return abort_flag() + 4 + 33 * (C::kIn + j); }
 };
 
 // Element pos of a tile: from the stage buffer below `bulk`, from global
@@ -159,6 +181,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     constexpr int NW = C::kWarps, ITEMS = C::kItems, TILE = C::kTile;
     constexpr int SIN = C::kIn, SOUT = C::kOut, RING = C::kRing, LW = C::kLookers;
     constexpr int WE = C::kWarpElems;
+    constexpr int AHEAD = C::kAhead;
     constexpr uint32_t NCONS = C::kConsumers;
     constexpr uint32_t kReducer0 = 1, kLooker0 = 1 + SIN, kReloader = 1 + SIN + LW,
                        kConsumer0 = 2 + SIN + LW;
@@ -199,28 +222,57 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         // ------------------------------------------------------- producer
         // Tile indices come from the atomic counter in the order tiles start
         // ("Scanning a whole array: three grid strategies"), so a tile only
-        // ever waits for tiles that some running block already holds.
+        // ever waits for tiles that some running block already holds. The
+        // tile of iteration k is taken AHEAD iterations before its input
+        // stage frees up and L2 is asked to fetch it meanwhile: the bulk load
+        // then finds it there, and a stage is held for a shorter time.
         if (lane != 0) return;
+        const uint64_t keep = l2_policy_evict_last();
+        uint32_t taken = 0;  // iterations whose tile index has been drawn
+        bool drawn_all = false;
         for (uint32_t k = 0;; ++k) {
             const int s = int(k % SIN), i = int(k % RING);
-            if ((k >= uint32_t(SIN) &&
-                 !mbar_wait(sm.in_empty(s), ((k / SIN) - 1) & 1u, kPipeWaitLimit)) ||
-                (k >= uint32_t(RING) &&
-                 !mbar_wait(sm.info_free(i), ((k / RING) - 1) & 1u, kPipeWaitLimit))) {
+            bool ok = true;
+            while (ok && !drawn_all && taken <= k + uint32_t(AHEAD)) {
+                const uint32_t g = taken;
+                const int gi = int(g % RING);
+                if (g >= uint32_t(RING) &&
+                    !mbar_wait(sm.info_free(gi), ((g / RING) - 1) & 1u, kPipeWaitLimit)) {
+                    ok = false;
+                    break;
+                }
+                uint32_t t = kNoTile;
+                if (ld_volatile_smem(sm.abort_flag()) == 0) {
+                    t = atomicAdd(&hdr->tile_counter, 1u);
+                    if (t >= num_tiles) t = kNoTile;
+                }
+                *reinterpret_cast<volatile uint32_t *>(sm.tile_id(gi)) = t;
+                ++taken;
+                if (t == kNoTile) {
+                    // iteration g carries the sentinel down the pipeline;
+                    // warps waiting for later iterations see end_iter < their k
+                    drawn_all = true;
+                    stop_at(g);
+                } else if (AHEAD > 0) {
+                    uint32_t valid, bulk;
+                    tile_extent(t, valid, bulk);
+                    if (bulk) bulk_prefetch_l2(in + uint64_t(t) * TILE, bulk * 4u, keep);
+                }
+            }
+            if (ok && k >= uint32_t(SIN))
+                ok = mbar_wait(sm.in_empty(s), ((k / SIN) - 1) & 1u, kPipeWaitLimit);
+            if (!ok) {
                 record_error(hdr, DWP_ERR_PIPELINE_TIMEOUT);
+                // tiles drawn but never loaded: poison them so no successor waits
+                for (uint32_t g = k; g < taken; ++g) {
+                    const uint32_t t = ld_volatile_smem(sm.tile_id(int(g % RING)));
+                    if (t != kNoTile) st_relaxed_gpu(desc + t, make_desc(kPoison, 0u));
+                }
                 stop_at(k - 1);  // buffers still in use: leave them alone
                 return;
             }
-            uint32_t t = kNoTile;
-            if (ld_volatile_smem(sm.abort_flag()) == 0) {
-                t = atomicAdd(&hdr->tile_counter, 1u);
-                if (t >= num_tiles) t = kNoTile;
-            }
-            *reinterpret_cast<volatile uint32_t *>(sm.tile_id(i)) = t;
+            const uint32_t t = ld_volatile_smem(sm.tile_id(i));
             if (t == kNoTile) {
-                // iteration k carries the sentinel down the pipeline; warps
-                // waiting for later iterations see end_iter < their k
-                stop_at(k);
                 mbar_arrive(sm.in_full(s));
                 return;
             }
@@ -228,8 +280,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             tile_extent(t, valid, bulk);
             if (bulk) {
                 mbar_arrive_expect_tx(sm.in_full(s), bulk * 4u);
-                bulk_load_hint(sm.in_data(s), in + uint64_t(t) * TILE, bulk * 4u, sm.in_full(s),
-                               l2_policy_evict_last());
+                bulk_load_hint(sm.in_data(s), in + uint64_t(t) * TILE, bulk * 4u, sm.in_full(s), keep);
             } else {
                 mbar_arrive(sm.in_full(s));
             }
@@ -268,7 +319,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             const uint64_t base = uint64_t(t) * TILE;
             const uint32_t *buf = sm.in_data(s);
             uint32_t *pre = sm.prefix(i);
-            uint32_t *lt = sm.lane_tot(i);
+            uint32_t *lt = sm.lane_tot(s);
             // totals of consumer threads c = lane + 32*w, whose ITEMS
             // contiguous elements start at c*ITEMS
             T tot[NW];
@@ -358,7 +409,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             T carry = Op::identity();
             int rc = (draining || ld_volatile_smem(sm.lbres(i)) != 0u) ? 1 : 0;
             if (rc == 0 && t != 0)
-                rc = lookback<Op, C::kLookK>(desc, t, lane, fault.spin_limit, sm.lb_scratch(i), &carry);
+                rc = lookback<Op, C::kLookK>(desc, t, lane, fault.spin_limit, sm.lb_scratch(int(j)), &carry);
             if (lane == 0) {
                 if (rc == 0) {
                     if (t != 0 && t != fault.never_publish_tile)
