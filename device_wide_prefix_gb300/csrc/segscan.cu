@@ -9,8 +9,9 @@
 //     (h1, v1) (+) (h2, v2) = (h1 | h2, h2 ? v2 : v1 + v2),
 // an associative, non-commutative operator.
 //
-// The pipeline is the plain scan's (scan.cu): producer warp with bulk loads
-// into SIN input stages; reducer warps that free their input stage as soon
+// The pipeline is the plain scan's (scan.cu): producer warp that draws tile
+// indices AHEAD iterations early, prefetches those tiles into L2, and bulk
+// loads them into SIN input stages; reducer warps that free their input stage as soon
 // as the tile is reduced; a pool of look-back warps; a reloader warp that
 // brings a tile back from L2 once its carry is known; consumer warps with
 // per-warp bulk stores.  What differs:
@@ -40,7 +41,7 @@ namespace {
 
 constexpr int kSample = 2048;  // offsets sampled into shared memory per block
 
-template <int NW_, int ITEMS_, int SIN_, int SOUT_, int RING_, int LW_, int LOOKK_>
+template <int NW_, int ITEMS_, int SIN_, int SOUT_, int RING_, int LW_, int LOOKK_, int AHEAD_>
 struct SegConfig {
     static constexpr int kWarps = NW_;
     static constexpr int kItems = ITEMS_;
@@ -49,6 +50,7 @@ struct SegConfig {
     static constexpr int kRing = RING_;
     static constexpr int kLookers = LW_;
     static constexpr int kLookK = LOOKK_;
+    static constexpr int kAhead = AHEAD_;  // iterations a tile index is drawn before its load
     static constexpr int kThreads = (2 + SIN_ + LW_ + NW_) * 32;
     static constexpr int kConsumers = NW_ * 32;
     static constexpr int kWarpElems = 32 * ITEMS_;
@@ -58,6 +60,7 @@ struct SegConfig {
     static_assert(NW_ >= 1 && NW_ <= 32, "");
     static_assert(RING_ % LW_ == 0, "a look-back warp must own every use of its info slots");
     static_assert(SOUT_ >= 2, "the reloader waits for the output stage of iteration k - SOUT");
+    static_assert(RING_ >= SIN_ + SOUT_ + 2 + AHEAD_, "info ring shorter than the work in flight");
     static constexpr size_t kStageBytes = size_t(kTile) * 4;
     static constexpr int kPrefixWords = kConsumers + kConsumers / 8;
     static constexpr int kPHeadWords = kConsumers / 4;  // one head byte per consumer thread
@@ -73,6 +76,8 @@ struct SegConfig {
     // + abort, end, cover lo, cover hi, then the offset sample
     static constexpr size_t kSmemBytes = kStageBytes * (SIN_ + SOUT_) + kInfoBytes * RING_ +
                                          kBarBytes + 16 + 4 * kSample;
+    static_assert(kThreads <= 1024, "more than 1024 threads per block");
+    static_assert(kSmemBytes <= 232448, "more than 227 KiB of shared memory per block");
 };
 
 #ifndef DWP_SEG_WARPS
@@ -96,8 +101,11 @@ struct SegConfig {
 #ifndef DWP_SEG_LOOKK
 #define DWP_SEG_LOOKK 1
 #endif
+#ifndef DWP_SEG_AHEAD
+#define DWP_SEG_AHEAD 1
+#endif
 using SegCfg = SegConfig<DWP_SEG_WARPS, DWP_SEG_ITEMS, DWP_SEG_IN, DWP_SEG_OUT, DWP_SEG_RING,
-                         DWP_SEG_LOOKERS, DWP_SEG_LOOKK>;
+                         DWP_SEG_LOOKERS, DWP_SEG_LOOKK, DWP_SEG_AHEAD>;
 
 template <class C>
 struct SegSmem {
@@ -197,6 +205,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     constexpr int NW = C::kWarps, ITEMS = C::kItems, TILE = C::kTile;
     constexpr int SIN = C::kIn, SOUT = C::kOut, RING = C::kRing, LW = C::kLookers;
     constexpr int WE = C::kWarpElems;
+    constexpr int AHEAD = C::kAhead;
     constexpr uint32_t NCONS = C::kConsumers;
     constexpr uint32_t kReducer0 = 1, kLooker0 = 1 + SIN, kReloader = 1 + SIN + LW,
                        kConsumer0 = 2 + SIN + LW;
@@ -245,26 +254,54 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------- producer
+        // As in the plain scan: the tile of iteration k is drawn AHEAD
+        // iterations early and prefetched into L2, so its bulk load is short.
         if (lane != 0) return;
+        const uint64_t keep = l2_policy_evict_last();
+        uint32_t taken = 0;  // iterations whose tile index has been drawn
+        bool drawn_all = false;
         for (uint32_t k = 0;; ++k) {
             const int s = int(k % SIN), i = int(k % RING);
-            if ((k >= uint32_t(SIN) &&
-                 !mbar_wait(sm.in_empty(s), ((k / SIN) - 1) & 1u, kPipeWaitLimit)) ||
-                (k >= uint32_t(RING) &&
-                 !mbar_wait(sm.info_free(i), ((k / RING) - 1) & 1u, kPipeWaitLimit))) {
+            bool ok = true;
+            while (ok && !drawn_all && taken <= k + uint32_t(AHEAD)) {
+                const uint32_t g = taken;
+                const int gi = int(g % RING);
+                if (g >= uint32_t(RING) &&
+                    !mbar_wait(sm.info_free(gi), ((g / RING) - 1) & 1u, kPipeWaitLimit)) {
+                    ok = false;
+                    break;
+                }
+                uint32_t t = kNoTile;
+                if (ld_volatile_smem(sm.abort_flag()) == 0) {
+                    t = atomicAdd(&hdr->tile_counter, 1u);
+                    if (t >= num_tiles) t = kNoTile;
+                }
+                *reinterpret_cast<volatile uint32_t *>(sm.tile_id(gi)) = t;
+                ++taken;
+                if (t == kNoTile) {
+                    drawn_all = true;
+                    stop_at(g);
+                } else if (AHEAD > 0) {
+                    uint32_t valid, bulk;
+                    tile_extent(t, valid, bulk);
+                    if (bulk) bulk_prefetch_l2(in + uint64_t(t) * TILE, bulk * 4u, keep);
+                }
+            }
+            if (ok && k >= uint32_t(SIN))
+                ok = mbar_wait(sm.in_empty(s), ((k / SIN) - 1) & 1u, kPipeWaitLimit);
+            if (!ok) {
                 record_error(hdr, DWP_ERR_PIPELINE_TIMEOUT);
+                // tiles drawn but never loaded: poison them so no successor waits
+                for (uint32_t g = k; g < taken; ++g) {
+                    const uint32_t t = ld_volatile_smem(sm.tile_id(int(g % RING)));
+                    if (t != kNoTile) st_relaxed_gpu(desc + t, make_desc(kPoison, 0u));
+                }
                 stop_at(k - 1);
                 return;
             }
-            uint32_t t = kNoTile;
-            if (ld_volatile_smem(sm.abort_flag()) == 0) {
-                t = atomicAdd(&hdr->tile_counter, 1u);
-                if (t >= num_tiles) t = kNoTile;
-            }
-            *reinterpret_cast<volatile uint32_t *>(sm.tile_id(i)) = t;
+            const uint32_t t = ld_volatile_smem(sm.tile_id(i));
             mbar_arrive(sm.id_ready(s));  // heads can be marked while the data is in flight
             if (t == kNoTile) {
-                stop_at(k);
                 mbar_arrive(sm.in_full(s));
                 return;
             }
@@ -272,8 +309,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             tile_extent(t, valid, bulk);
             if (bulk) {
                 mbar_arrive_expect_tx(sm.in_full(s), bulk * 4u);
-                bulk_load_hint(sm.in_data(s), in + uint64_t(t) * TILE, bulk * 4u, sm.in_full(s),
-                               l2_policy_evict_last());
+                bulk_load_hint(sm.in_data(s), in + uint64_t(t) * TILE, bulk * 4u, sm.in_full(s), keep);
             } else {
                 mbar_arrive(sm.in_full(s));
             }
