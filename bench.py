@@ -405,9 +405,54 @@ def measure_secondary(dwp, lib, dev, stream, peaks, x, y, scratch, need) -> dict
         out[name] = {"n": n, "ms": ms, "Gelem_s": n / (ms * 1e-3) / 1e9, "GB_s": gbs,
                      "frac": gbs / peaks["hbm_gbs"]}
     del xf
+    out["u32_add_exclusive_2p20"] = measure_small(dwp, lib, dev, stream)
+    out["fallback_one_silent_tile"] = measure_fallback(dwp, lib, stream, x, y, scratch, need)
     out["segscan_u32_exclusive"] = measure_segscan(dwp, lib, dev, stream, peaks)
     out["compact_16B_records"] = measure_compact(dwp, lib, dev, stream, peaks)
     return out
+
+
+def measure_small(dwp, lib, dev, stream, log2n=20, steps=2000, warmup=20) -> dict:
+    """The small case: u32 exclusive add over 2^20 values in [0, 16), L2-resident
+    and launch-bound, so the figure is microseconds per call."""
+    import ctypes
+    import torch
+    n = 1 << log2n
+    x = torch.from_numpy(synth.u32_small_values(n).view(np.int32)).to(dev)
+    y = torch.empty_like(x)
+    sb = ctypes.c_size_t(0)
+    lib.dwp_scan_exclusive(0, None, None, n, None, ctypes.byref(sb), None)
+    scratch = torch.empty(sb.value, dtype=torch.uint8, device=dev)
+    args = (dwp.DWP_U32_ADD, ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(y.data_ptr()), n,
+            ctypes.c_void_p(scratch.data_ptr()), ctypes.byref(sb),
+            ctypes.c_void_p(int(stream.cuda_stream)))
+    ms = time_calls(lambda: lib.dwp_scan_exclusive(*args), steps, warmup, stream)
+    return {"n": n, "us": ms * 1e3, "Gelem_s": n / (ms * 1e-3) / 1e9,
+            "workload": "u32 exclusive sum scan, n=2^%d values in [0,16) (SplitMix64 seed 0xD3B00001), "
+                        "L2-resident: launch-bound, not an HBM figure" % log2n}
+
+
+def measure_fallback(dwp, lib, stream, x, y, scratch, need, silent=5, polls=64, steps=20) -> dict:
+    """Cost of one Decoupled Fallback: the headline call with tile `silent`
+    never publishing, its successors rescuing it after `polls` look-back polls."""
+    import ctypes
+    n = x.numel()
+    sb = ctypes.c_size_t(need)
+    st_ptr = ctypes.c_void_p(int(stream.cuda_stream))
+    args = (dwp.DWP_U32_ADD, ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(y.data_ptr()), n,
+            ctypes.c_void_p(scratch.data_ptr()), ctypes.byref(sb), st_ptr)
+    healthy = time_calls(lambda: lib.dwp_scan_exclusive(*args), steps, 3, stream)
+    try:
+        lib.dwp_debug_set_fault(silent, 0, polls)
+        ms = time_calls(lambda: lib.dwp_scan_exclusive(*args), steps, 3, stream)
+        status = lib.dwp_read_status(ctypes.c_void_p(scratch.data_ptr()), st_ptr)
+        fb = ctypes.c_uint32(0)
+        lib.dwp_read_fallbacks(ctypes.c_void_p(scratch.data_ptr()), st_ptr, ctypes.byref(fb))
+    finally:
+        lib.dwp_debug_set_fault(0xFFFFFFFF, 0, 0)
+    return {"n": n, "silent_tile": silent, "fallback_polls": polls, "ms": ms,
+            "healthy_ms": healthy, "added_us": (ms - healthy) * 1e3, "fallbacks_last_call": fb.value,
+            "status": dwp.dwp_status_string(status)}
 
 
 def run_only(args) -> None:

@@ -45,6 +45,7 @@ EXPORTS = [
     "dwp_segmented_scan_u32",
     "dwp_compact_by_flags",
     "dwp_read_status",
+    "dwp_read_fallbacks",
     "dwp_status_string",
     "dwp_version",
     "dwp_debug_set_fault",
@@ -82,11 +83,13 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dwp_compact_by_flags.restype = c.c_int
     lib.dwp_read_status.argtypes = [P, P]
     lib.dwp_read_status.restype = c.c_int
+    lib.dwp_read_fallbacks.argtypes = [P, P, c.POINTER(c.c_uint32)]
+    lib.dwp_read_fallbacks.restype = c.c_int
     lib.dwp_status_string.argtypes = [c.c_int]
     lib.dwp_status_string.restype = c.c_char_p
     lib.dwp_version.argtypes = []
     lib.dwp_version.restype = c.c_int
-    lib.dwp_debug_set_fault.argtypes = [c.c_uint32, c.c_uint32]
+    lib.dwp_debug_set_fault.argtypes = [c.c_uint32, c.c_uint32, c.c_uint32]
     lib.dwp_debug_set_fault.restype = c.c_int
     lib.dwp_scan_static_scratch.argtypes = [c.c_int, c.c_int, P, P, S, P]
     lib.dwp_scan_static_scratch.restype = c.c_int
@@ -146,6 +149,13 @@ def dwp_read_status(d_scratch, stream) -> int:
     return load().dwp_read_status(d_scratch or None, stream or None)
 
 
+def dwp_read_fallbacks(d_scratch, stream):
+    """(status, count of Decoupled Fallbacks the last call on d_scratch made)."""
+    v = ctypes.c_uint32(0)
+    st = load().dwp_read_fallbacks(d_scratch or None, stream or None, ctypes.byref(v))
+    return st, v.value
+
+
 def dwp_status_string(status: int) -> str:
     return load().dwp_status_string(int(status)).decode()
 
@@ -154,8 +164,9 @@ def dwp_version() -> int:
     return load().dwp_version()
 
 
-def dwp_debug_set_fault(never_publish_tile: int, spin_limit: int) -> int:
-    return load().dwp_debug_set_fault(never_publish_tile & 0xFFFFFFFF, spin_limit)
+def dwp_debug_set_fault(never_publish_tile: int, spin_limit: int, fallback_polls: int = 0) -> int:
+    return load().dwp_debug_set_fault(never_publish_tile & 0xFFFFFFFF, spin_limit,
+                                      fallback_polls & 0xFFFFFFFF)
 
 
 def status_string(status: int) -> str:
@@ -300,3 +311,11 @@ def compact_by_flags(records, flags, out=None, count=None, scratch=None, stream=
 def read_status(scratch, stream=None) -> int:
     """Device-side status of the last call that used `scratch` (synchronises)."""
     return dwp_read_status(scratch.data_ptr(), _stream_of(scratch, stream))
+
+
+def read_fallbacks(scratch, stream=None) -> int:
+    """Tiles whose aggregate a waiting successor computed itself (Decoupled
+    Fallback) in the last call that used `scratch` (synchronises)."""
+    st, v = dwp_read_fallbacks(scratch.data_ptr(), _stream_of(scratch, stream))
+    _check(st, "dwp_read_fallbacks")
+    return v

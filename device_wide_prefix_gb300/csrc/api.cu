@@ -199,8 +199,23 @@ const char *dwp_status_string(dwp_status status) {
 
 int dwp_version(void) { return 100; }
 
-dwp_status dwp_debug_set_fault(uint32_t never_publish_tile, uint32_t spin_limit) {
-    set_fault_config(never_publish_tile, spin_limit);
+dwp_status dwp_read_fallbacks(const void *d_scratch, dwp_stream stream, uint32_t *count) {
+    if (!d_scratch || !count) return DWP_ERR_INVALID_VALUE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t v = 0;
+    const auto *hdr = reinterpret_cast<const ScratchHeader *>(d_scratch);
+    if (cudaMemcpyAsync(&v, &hdr->fallbacks, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return DWP_ERR_CUDA;
+    }
+    *count = v;
+    return DWP_SUCCESS;
+}
+
+dwp_status dwp_debug_set_fault(uint32_t never_publish_tile, uint32_t spin_limit,
+                               uint32_t fallback_polls) {
+    set_fault_config(never_publish_tile, spin_limit, fallback_polls);
     return DWP_SUCCESS;
 }
 

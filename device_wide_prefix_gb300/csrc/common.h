@@ -13,7 +13,8 @@ namespace dwp {
 struct ScratchHeader {
     uint32_t tile_counter;  // next tile index to hand out (atomicAdd)
     uint32_t status;        // 0, or the first device-side dwp_status recorded
-    uint32_t reserved[30];
+    uint32_t fallbacks;     // tiles whose aggregate a successor computed and published
+    uint32_t reserved[29];
 };
 static_assert(sizeof(ScratchHeader) == 128, "scratch header is 128 bytes");
 
@@ -25,14 +26,19 @@ inline size_t scratch_bytes_for_tiles(uint64_t tiles) { return kHeaderBytes + 8u
 // error and the kernel exits instead of hanging.
 constexpr uint32_t kDefaultSpinLimit = 1u << 20;  // look-back polls (~1 s with backoff)
 constexpr uint32_t kPipeWaitLimit = 1u << 24;     // mbarrier polls (>1 s with backoff)
+// Look-back polls on a window with an unpublished predecessor before the
+// waiting tile reduces that predecessor itself (several ms with backoff:
+// far above any wait of a healthy run).
+constexpr uint32_t kDefaultFallbackPolls = 1u << 12;
 
 // Test hooks carried into every launch (see dwp_debug_set_fault).
 struct FaultConfig {
     uint32_t never_publish_tile;  // UINT32_MAX: none
     uint32_t spin_limit;          // look-back polls before giving up
+    uint32_t fallback_polls;      // polls before a Decoupled Fallback; 0: never
 };
 
 FaultConfig current_fault_config();
-void set_fault_config(uint32_t never_publish_tile, uint32_t spin_limit);
+void set_fault_config(uint32_t never_publish_tile, uint32_t spin_limit, uint32_t fallback_polls);
 
 }  // namespace dwp

@@ -131,6 +131,34 @@ __device__ __forceinline__ bool keep_at(const unsigned char *sflags, const uint8
     return false;
 }
 
+// Decoupled Fallback for compaction: the descriptor tile p would publish,
+// the number of nonzero flags among its records, counted by one warp from
+// the flag bytes (tile 0's count is its inclusive prefix).
+template <int TILE>
+struct CompactRescue {
+    static_assert(TILE % 16 == 0, "full tiles are read as 16-byte vectors");
+    const uint8_t *flags;
+    uint64_t n;
+    __device__ uint64_t operator()(uint32_t p, uint32_t lane, uint32_t *) const {
+        const uint64_t b = uint64_t(p) * TILE;
+        const uint64_t e = min(n, b + uint64_t(TILE));
+        uint32_t cnt = 0;
+        if (e - b == uint64_t(TILE)) {
+            const uint4 *v4 = reinterpret_cast<const uint4 *>(flags + b);
+            for (uint32_t q = lane; q < uint32_t(TILE) / 16u; q += 32u) {
+                const uint4 v = v4[q];
+                // __vcmpne4: 0xff in every nonzero byte
+                cnt += (__popc(__vcmpne4(v.x, 0u)) + __popc(__vcmpne4(v.y, 0u)) +
+                        __popc(__vcmpne4(v.z, 0u)) + __popc(__vcmpne4(v.w, 0u))) >> 3;
+            }
+        } else {
+            for (uint64_t q = b + lane; q < e; q += 32u) cnt += flags[q] != 0 ? 1u : 0u;
+        }
+        cnt = __reduce_add_sync(0xffffffffu, cnt);
+        return make_desc(p == 0 ? kPrefix : kAggregate, cnt);
+    }
+};
+
 template <class C>
 __global__ void __launch_bounds__(C::kThreads, 1)
     compact_kernel(const uint4 *recs, const uint8_t *flags, uint64_t n, uint4 *out,
@@ -277,7 +305,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             uint32_t carry = 0;
             int rc = 0;
             if (t != 0)
-                rc = lookback<Op, C::kLookK>(desc, t, lane, fault.spin_limit, sm.lb_scratch(i), &carry);
+                rc = lookback<Op, C::kLookK>(desc, t, lane, fault.spin_limit, fault.fallback_polls,
+                                             CompactRescue<TILE>{flags, n}, &hdr->fallbacks,
+                                             sm.lb_scratch(i), &carry);
             if (lane == 0) {
                 if (rc == 0) {
                     if (t != 0 && t != fault.never_publish_tile)

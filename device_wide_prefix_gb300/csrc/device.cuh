@@ -291,13 +291,27 @@ __device__ __forceinline__ int warp_wait_or_end(uint64_t *bar, uint32_t parity, 
 // Warp collectives are kept to a few per poll: on a GB300 streaming at full
 // bandwidth each one was measured at several hundred cycles.
 //
+// Decoupled Fallback ("GPU Prefix Sums", section "Decoupled Fallback"): with
+// fallback_polls > 0, once a window has been polled fallback_polls times with
+// a predecessor still unpublished, the warp stops waiting for it.  For each
+// such predecessor p, `rescue(p, lane, scratch)` (called by all 32 lanes,
+// same result on each) reduces tile p straight from the input and returns
+// the descriptor p would publish; lane 0 installs it with a compare-and-swap
+// against the invalid state.  So of several rescuers and the tile's own
+// block, whichever writes first wins, and a lost swap hands back the winning
+// descriptor (the same value for the integer operators; for f32 another
+// grouping of the same sum).  Each swap won adds one to *fallbacks.  The
+// input must stay unmodified for the whole launch: callers disable the
+// fallback (fallback_polls = 0) for an in-place scan.
+//
 // Returns 0 and the exclusive prefix of tile t in *carry_out; 1 if the
 // nearest terminal descriptor is poison; 2 if the poll limit ran out.
 
-template <class Op, int K>
-__device__ __forceinline__ int lookback(const uint64_t *desc, uint32_t t, uint32_t lane,
-                                        uint32_t spin_limit, uint32_t *scratch,
-                                        typename Op::T *carry_out) {
+template <class Op, int K, class Rescue>
+__device__ __forceinline__ int lookback(uint64_t *desc, uint32_t t, uint32_t lane,
+                                        uint32_t spin_limit, uint32_t fallback_polls,
+                                        const Rescue &rescue, uint32_t *fallbacks,
+                                        uint32_t *scratch, typename Op::T *carry_out) {
     using T = typename Op::T;
     static_assert(Op::kCommutative, "the look-back combines per lane first");
     static_assert(K * 32 < (1 << 30), "window positions must fit the key");
@@ -312,7 +326,7 @@ __device__ __forceinline__ int lookback(const uint64_t *desc, uint32_t t, uint32
             d[i] = idx >= 0 ? ld_relaxed_gpu(desc + idx)
                             : make_desc(kPrefix, Op::to_bits(Op::identity()));
         }
-        uint32_t tkey, imin;
+        uint32_t tkey, imin, stalled = 0;
         while (true) {
             // key of the nearest terminal descriptor = 2*position + poison bit
             uint32_t my_t = 0xffffffffu, my_i = 0xffffffffu;
@@ -327,8 +341,34 @@ __device__ __forceinline__ int lookback(const uint64_t *desc, uint32_t t, uint32
             imin = __reduce_min_sync(0xffffffffu, my_i);
             if (tkey != 0xffffffffu ? imin > (tkey >> 1) : imin == 0xffffffffu) break;
             if (++polls >= spin_limit) return 2;
-            if (polls > 8) __nanosleep(polls > 256 ? 256 : 64);
             const uint32_t lim = tkey != 0xffffffffu ? (tkey >> 1) : 32u * K;
+            if (fallback_polls != 0u && ++stalled >= fallback_polls) {
+                stalled = 0;
+#pragma unroll
+                for (int i = 0; i < K; ++i) {
+                    const int64_t idx = base - 32 * i - static_cast<int64_t>(lane);
+                    uint32_t need = __ballot_sync(
+                        0xffffffffu, 32u * i + lane < lim && idx >= 0 && desc_state(d[i]) == kInvalid);
+                    while (need) {
+                        const uint32_t j = uint32_t(__ffs(need)) - 1u;
+                        need &= need - 1u;
+                        const uint32_t p = static_cast<uint32_t>(base - 32 * i - static_cast<int64_t>(j));
+                        const uint64_t mine = rescue(p, lane, scratch);
+                        unsigned long long got = 0ull;
+                        if (lane == 0) {
+                            const unsigned long long old = atomicCAS(
+                                reinterpret_cast<unsigned long long *>(desc + p), 0ull,
+                                static_cast<unsigned long long>(mine));
+                            got = old == 0ull ? static_cast<unsigned long long>(mine) : old;
+                            if (old == 0ull) atomicAdd(fallbacks, 1u);
+                        }
+                        got = __shfl_sync(0xffffffffu, got, 0);
+                        if (lane == j) d[i] = got;
+                    }
+                }
+                continue;
+            }
+            if (polls > 8) __nanosleep(polls > 256 ? 256 : 64);
 #pragma unroll
             for (int i = 0; i < K; ++i) {
                 const int64_t idx = base - 32 * i - static_cast<int64_t>(lane);

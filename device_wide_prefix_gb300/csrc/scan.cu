@@ -173,6 +173,34 @@ __device__ __forceinline__ typename Op::T tile_elem(const uint32_t *buf, const t
     return Op::identity();
 }
 
+// Decoupled Fallback for the plain scan: the descriptor tile p would
+// publish, reduced by one warp straight from the input (tile 0's aggregate
+// is its inclusive prefix).
+template <class Op, int TILE>
+struct ScanRescue {
+    static_assert(TILE % 4 == 0, "full tiles are read as 16-byte vectors");
+    const typename Op::T *in;
+    uint64_t n;
+    __device__ uint64_t operator()(uint32_t p, uint32_t lane, uint32_t *scratch) const {
+        using T = typename Op::T;
+        const uint64_t b = uint64_t(p) * TILE;
+        const uint64_t e = min(n, b + uint64_t(TILE));
+        T acc = Op::identity();
+        if (e - b == uint64_t(TILE)) {
+            const uint4 *v4 = reinterpret_cast<const uint4 *>(in + b);
+            for (uint32_t q = lane; q < uint32_t(TILE) / 4u; q += 32u) {
+                const uint4 v = v4[q];
+                acc = Op::combine(acc, Op::combine(Op::combine(Op::from_bits(v.x), Op::from_bits(v.y)),
+                                                   Op::combine(Op::from_bits(v.z), Op::from_bits(v.w))));
+            }
+        } else {
+            for (uint64_t q = b + lane; q < e; q += 32u) acc = Op::combine(acc, in[q]);
+        }
+        const T tot = Op::warp_reduce(acc, lane, scratch);
+        return make_desc(p == 0 ? kPrefix : kAggregate, Op::to_bits(tot));
+    }
+};
+
 template <class Op, bool INCL, class C>
 __global__ void __launch_bounds__(C::kThreads, 1)
     scan_kernel(const typename Op::T *in, typename Op::T *out, uint64_t n, uint32_t num_tiles,
@@ -409,7 +437,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             T carry = Op::identity();
             int rc = (draining || ld_volatile_smem(sm.lbres(i)) != 0u) ? 1 : 0;
             if (rc == 0 && t != 0)
-                rc = lookback<Op, C::kLookK>(desc, t, lane, fault.spin_limit, sm.lb_scratch(int(j)), &carry);
+                rc = lookback<Op, C::kLookK>(desc, t, lane, fault.spin_limit, fault.fallback_polls,
+                                             ScanRescue<Op, TILE>{in, n}, &hdr->fallbacks,
+                                             sm.lb_scratch(int(j)), &carry);
             if (lane == 0) {
                 if (rc == 0) {
                     if (t != 0 && t != fault.never_publish_tile)
@@ -592,7 +622,9 @@ uint32_t scan_tile_elems() { return ScanCfg::kTile; }
 
 cudaError_t launch_scan(dwp_op op, bool inclusive, const void *in, void *out, uint64_t n,
                         void *scratch, cudaStream_t stream) {
-    const FaultConfig fault = current_fault_config();
+    FaultConfig fault = current_fault_config();
+    // in place, the input of a stalled tile may already be output: no fallback
+    if (in == out) fault.fallback_polls = 0u;
     switch (op) {
         case DWP_U32_ADD:
             return inclusive ? launch_one<OpU32Add, true>(in, out, n, scratch, stream, fault)

@@ -196,6 +196,39 @@ __device__ __forceinline__ uint32_t warp_lower_bound(const uint32_t *off, uint32
     return lo;
 }
 
+// Decoupled Fallback for the segmented scan: the descriptor tile p would
+// publish, from the values and the offsets.  The heads of a tile are the
+// offset values inside it; offsets are nondecreasing, so its last head is the
+// last offset below the tile end, if that offset is not below the tile
+// start.  A tile with a head publishes its prefix, the sum from its last head
+// to its end; a tile without one publishes the sum of its rows as its
+// aggregate; tile 0 always publishes a prefix.
+struct SegRescue {
+    const uint32_t *in;
+    const uint32_t *off;
+    uint32_t nseg;
+    uint64_t n;
+    uint32_t tile;
+    __device__ uint64_t operator()(uint32_t p, uint32_t lane, uint32_t *) const {
+        const uint64_t b = uint64_t(p) * tile;
+        const uint64_t e = min(n, b + uint64_t(tile));  // e <= n < 2^32
+        const uint32_t k = warp_lower_bound(off, 0u, nseg + 1u, uint32_t(e), lane);
+        uint64_t from = b;
+        bool head = false;
+        if (k > 0u) {
+            const uint32_t h = __ldg(off + k - 1u);
+            if (uint64_t(h) >= b) {
+                head = true;
+                from = h;
+            }
+        }
+        uint32_t acc = 0;
+        for (uint64_t q = from + lane; q < e; q += 32u) acc += __ldg(in + q);
+        acc = __reduce_add_sync(0xffffffffu, acc);
+        return make_desc((p == 0 || head) ? kPrefix : kAggregate, acc);
+    }
+};
+
 template <bool INCL, class C>
 __global__ void __launch_bounds__(C::kThreads, 1)
     segscan_kernel(const uint32_t *in, const uint32_t *off, uint32_t nseg, uint32_t *out,
@@ -513,7 +546,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             int rc = (draining || ld_volatile_smem(sm.lbres(i)) != 0u) ? 1 : 0;
             const bool ah = ld_volatile_smem(sm.agg_head(i)) != 0u;
             if (rc == 0 && t != 0 && ld_volatile_smem(sm.first_head(i)) == 0u)
-                rc = lookback<Op, C::kLookK>(desc, t, lane, fault.spin_limit, sm.lb_scratch(i), &carry);
+                rc = lookback<Op, C::kLookK>(desc, t, lane, fault.spin_limit, fault.fallback_polls,
+                                             SegRescue{in, off, nseg, n, uint32_t(TILE)},
+                                             &hdr->fallbacks, sm.lb_scratch(i), &carry);
             if (lane == 0) {
                 if (rc == 0) {
                     if (t != 0 && !ah && t != fault.never_publish_tile)

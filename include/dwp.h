@@ -193,6 +193,18 @@ dwp_status dwp_scan_static_scratch(dwp_op op, dwp_mode mode, const void *d_in, v
  */
 dwp_status dwp_read_status(const void *d_scratch, dwp_stream stream);
 
+/*
+ * Decoupled Fallback count of the most recent call that used d_scratch
+ * ("GPU Prefix Sums", section "Decoupled Fallback").  A tile whose
+ * look-back waits too long on a predecessor that has not published reduces
+ * that predecessor's input itself and publishes the result with a
+ * compare-and-swap; *count receives the number of such swaps that won.  It
+ * is 0 in a healthy run: the fallback starts only after thousands of polls
+ * (milliseconds).  Synchronises `stream`.  DWP_ERR_INVALID_VALUE for a NULL
+ * argument; DWP_ERR_CUDA if the synchronisation or the read fails.
+ */
+dwp_status dwp_read_fallbacks(const void *d_scratch, dwp_stream stream, uint32_t *count);
+
 /* Static, NUL-terminated name of a status code. */
 const char *dwp_status_string(dwp_status status);
 
@@ -201,14 +213,24 @@ int dwp_version(void);
 
 /*
  * Test hook, not for production use.  For every later call in this process
- * until reset: the tile with index `never_publish_tile` does its work but
- * never publishes its descriptor (UINT32_MAX disables this), and look-back
- * spins give up after `spin_limit` polls (0 restores the default, about a
- * second of polling).  The successors of the silent tile then record
- * DWP_ERR_LOOKBACK_TIMEOUT in the scratch status and exit instead of
- * waiting forever.  Not thread-safe; affects every device.
+ * until reset:
+ *   - the tile with index `never_publish_tile` does its work but never
+ *     publishes its descriptor (UINT32_MAX disables this);
+ *   - look-back spins give up after `spin_limit` polls (0 restores the
+ *     default, about a second of polling);
+ *   - a look-back takes the Decoupled Fallback after `fallback_polls` polls
+ *     on an unpublished predecessor (0 restores the default, 4096 polls;
+ *     UINT32_MAX disables the fallback).
+ * With the fallback on, the successors of the silent tile reduce its input
+ * themselves and the call succeeds with correct output (see
+ * dwp_read_fallbacks).  With it off, or for an in-place scan (where the
+ * fallback is always off: the silent tile's input may already have been
+ * overwritten), they record DWP_ERR_LOOKBACK_TIMEOUT in the scratch status
+ * and exit instead of waiting forever.  Not thread-safe; affects every
+ * device.
  */
-dwp_status dwp_debug_set_fault(uint32_t never_publish_tile, uint32_t spin_limit);
+dwp_status dwp_debug_set_fault(uint32_t never_publish_tile, uint32_t spin_limit,
+                               uint32_t fallback_polls);
 
 #ifdef __cplusplus
 }

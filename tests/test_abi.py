@@ -107,3 +107,7 @@ def test_null_scratch_bytes_pointer(lib):
     st = lib.dwp_scan_exclusive(0, None, None, 10, None, ctypes.POINTER(ctypes.c_size_t)(), None)
     assert st == dwp.DWP_ERR_INVALID_VALUE
     assert lib.dwp_read_status(None, None) == dwp.DWP_ERR_INVALID_VALUE
+    v = ctypes.c_uint32(7)
+    assert lib.dwp_read_fallbacks(None, None, ctypes.byref(v)) == dwp.DWP_ERR_INVALID_VALUE
+    assert lib.dwp_read_fallbacks(ctypes.c_void_p(4096), None, None) == dwp.DWP_ERR_INVALID_VALUE
+    assert v.value == 7

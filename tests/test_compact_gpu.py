@@ -119,3 +119,32 @@ def test_full_2p26_records_p03(ref):
     assert (got[:k] == want[:k]).all()
     ids = got[:k, 0].astype(np.int64)
     assert (np.diff(ids) > 0).all()  # stable: ids = input index, strictly increasing
+
+
+# ------------------------------------------------------- Decoupled Fallback
+
+@pytest.mark.parametrize("silent", [0, 7, 399])
+def test_fallback_rescues_a_silent_tile(ref, silent):
+    """Decoupled Fallback on compaction: a silent tile's kept count is
+    counted from its flags by a waiting successor; count and records exact."""
+    n = 400 * tile() - 9
+    rec = synth.records(n, seed=901)
+    flags = synth.keep_flags(n, 0.3, seed=902)
+    want, k = ref.compact(rec, flags)
+    r = torch.from_numpy(rec.view(np.int32)).cuda()
+    f = torch.from_numpy(flags).cuda()
+    out = torch.full_like(r, SENTINEL)
+    scratch = dwp.alloc_scratch(dwp.compact_scratch_bytes(n), r.device)
+    try:
+        dwp.dwp_debug_set_fault(silent, 0, 64)
+        out, cnt = dwp.compact_by_flags(r, f, out=out, scratch=scratch)
+        st = dwp.read_status(scratch)
+        fb = dwp.read_fallbacks(scratch)
+    finally:
+        dwp.dwp_debug_set_fault(0xFFFFFFFF, 0, 0)
+    assert st == dwp.DWP_SUCCESS
+    if silent < 399:
+        assert fb >= 1
+    got = out.cpu().numpy().view(np.uint32)
+    assert int(cnt.item()) == k
+    assert (got[:k] == want[:k]).all() and (got[k:] == SENTINEL).all()

@@ -173,17 +173,74 @@ def test_full_f32_inclusive_2p28(ref):
 # ---------------------------------------------------------------- failure path
 
 def test_lookback_timeout_is_reported_not_hung(ref):
-    """A tile that never publishes: its successors give up after a short spin,
-    record DWP_ERR_LOOKBACK_TIMEOUT and exit; the context stays usable."""
+    """A tile that never publishes, with the Decoupled Fallback off: its
+    successors give up after a short spin, record DWP_ERR_LOOKBACK_TIMEOUT
+    and exit; the context stays usable."""
     n = 2000 * tile()
     x = torch.from_numpy(synth.u32_small_values(n, 13).view(np.int32)).cuda()
     scratch = dwp.alloc_scratch(dwp.scan_scratch_bytes(n), x.device)
     try:
-        dwp.dwp_debug_set_fault(5, 2000)
+        dwp.dwp_debug_set_fault(5, 2000, 0xFFFFFFFF)
         dwp.scan_exclusive(x, "u32_add", scratch=scratch)
         assert dwp.read_status(scratch) == dwp.DWP_ERR_LOOKBACK_TIMEOUT
     finally:
-        dwp.dwp_debug_set_fault(0xFFFFFFFF, 0)
+        dwp.dwp_debug_set_fault(0xFFFFFFFF, 0, 0)
     y = dwp.scan_exclusive(x, "u32_add", scratch=scratch)
     assert dwp.read_status(scratch) == dwp.DWP_SUCCESS
     check(ref, x.cpu().numpy().view(np.uint32), "u32_add", False, y.cpu().numpy().view(np.uint32))
+
+
+# ------------------------------------------------------- Decoupled Fallback
+
+FALLBACK_POLLS = 64  # far below the default: the silent tile is rescued in microseconds
+
+
+@pytest.mark.parametrize("op,inclusive,silent", [
+    ("u32_add", False, 5), ("u32_add", True, 0), ("u32_max", False, 777),
+    ("f32_add", True, 1999)])
+def test_fallback_rescues_a_silent_tile(ref, op, inclusive, silent):
+    """Decoupled Fallback: a tile that never publishes is reduced by the
+    successors that wait for it; the call succeeds with the oracle's output
+    and reports at least one fallback.  Tile 0 is rescued as a prefix, the
+    last tile (1999, ragged) from its partial extent."""
+    n = 1999 * tile() + 1234
+    x = synth.f32_values(n, 21) if op == "f32_add" else synth.u32_full_values(n, 21)
+    t = torch.from_numpy(x.view(np.float32 if op == "f32_add" else np.int32)).cuda()
+    scratch = dwp.alloc_scratch(dwp.scan_scratch_bytes(n, op), t.device)
+    try:
+        dwp.dwp_debug_set_fault(silent, 0, FALLBACK_POLLS)
+        y = (dwp.scan_inclusive if inclusive else dwp.scan_exclusive)(t, op, scratch=scratch)
+        st = dwp.read_status(scratch)
+        fb = dwp.read_fallbacks(scratch)
+    finally:
+        dwp.dwp_debug_set_fault(0xFFFFFFFF, 0, 0)
+    assert st == dwp.DWP_SUCCESS
+    if silent < 1999:  # the last tile has no successor to rescue it
+        assert fb >= 1
+    check(ref, x, op, inclusive, y.cpu().numpy().view(x.dtype))
+
+
+def test_fallback_off_in_place(ref):
+    """In place the input of a silent tile may already be output, so the
+    fallback stays off and the timeout path reports the silent tile."""
+    n = 2000 * tile()
+    x = torch.from_numpy(synth.u32_small_values(n, 14).view(np.int32)).cuda()
+    scratch = dwp.alloc_scratch(dwp.scan_scratch_bytes(n), x.device)
+    try:
+        dwp.dwp_debug_set_fault(5, 2000, FALLBACK_POLLS)
+        dwp.scan_exclusive(x, "u32_add", out=x, scratch=scratch)
+        assert dwp.read_status(scratch) == dwp.DWP_ERR_LOOKBACK_TIMEOUT
+        assert dwp.read_fallbacks(scratch) == 0
+    finally:
+        dwp.dwp_debug_set_fault(0xFFFFFFFF, 0, 0)
+
+
+def test_no_fallback_in_a_healthy_run(ref):
+    """At the default threshold a healthy full-size run never falls back."""
+    n = 1 << 28
+    x = torch.from_numpy(synth.u32_full_values(n).view(np.int32)).cuda()
+    scratch = dwp.alloc_scratch(dwp.scan_scratch_bytes(n), x.device)
+    for _ in range(3):
+        dwp.scan_exclusive(x, "u32_add", scratch=scratch)
+        assert dwp.read_status(scratch) == dwp.DWP_SUCCESS
+        assert dwp.read_fallbacks(scratch) == 0

@@ -136,3 +136,41 @@ def test_full_skewed_2p27(ref, inclusive):
     n = 1 << 27
     off = synth.segment_offsets(n)
     check(ref, synth.u32_byte_values(n), off, inclusive)
+
+
+# ------------------------------------------------------- Decoupled Fallback
+
+def test_fallback_rescues_silent_tiles(ref):
+    """Decoupled Fallback on the segmented scan: a silent tile with heads (its
+    rescue publishes the sum after its last head as a prefix) and one without
+    (the rescue publishes its row sum as an aggregate); output bit-exact."""
+    T = tile()
+    n = 600 * T + 77
+    values = synth.u32_byte_values(n, seed=41)
+    offsets = synth.segment_offsets(n, seed=42)
+    starts = np.arange(0, n, T, dtype=np.int64)
+    heads = np.searchsorted(offsets, starts + T) - np.searchsorted(offsets, starts)
+    with_head = [int(i) for i in np.nonzero(heads > 0)[0] if 0 < i < starts.size - 1]
+    without = [int(i) for i in np.nonzero(heads == 0)[0] if 0 < i < starts.size - 1]
+    assert with_head and without
+    for silent in (with_head[len(with_head) // 2], without[len(without) // 2], 0):
+        want = ref.segmented_scan_u32(values, offsets, False, out=np.full(n, SENTINEL, np.uint32))
+        v = torch.from_numpy(values.view(np.int32)).cuda()
+        o = torch.from_numpy(offsets.astype(np.uint32).view(np.int32)).cuda()
+        out = torch.full((n,), SENTINEL - (1 << 32), dtype=torch.int32, device="cuda")
+        scratch = dwp.alloc_scratch(dwp.segmented_scan_scratch_bytes(n), v.device)
+        try:
+            dwp.dwp_debug_set_fault(silent, 0, 64)
+            dwp.segmented_scan(v, o, False, out=out, scratch=scratch)
+            st = dwp.read_status(scratch)
+            fb = dwp.read_fallbacks(scratch)
+        finally:
+            dwp.dwp_debug_set_fault(0xFFFFFFFF, 0, 0)
+        assert st == dwp.DWP_SUCCESS
+        got = out.cpu().numpy().view(np.uint32)
+        bad = np.nonzero(got != want)[0]
+        assert bad.size == 0, "silent %d: mismatch at %s" % (silent, bad[:5])
+        # the next tile looks back at the silent one unless its first row is
+        # a head (then no tile needs the silent tile's descriptor)
+        if not np.isin(starts[silent + 1], offsets):
+            assert fb >= 1
