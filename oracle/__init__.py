@@ -56,6 +56,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.oracle_segmented_scan_u32.restype = None
     lib.oracle_compact.argtypes = [c.c_void_p, _u8p, c.c_uint64, c.c_uint64, c.c_void_p]
     lib.oracle_compact.restype = c.c_uint64
+    lib.oracle_linear_recurrence_f32.argtypes = [_f32p, _f32p, c.c_uint64, c.c_int, _f64p, _f64p]
+    lib.oracle_linear_recurrence_f32.restype = None
     if path is None:
         _lib = lib
     return lib
@@ -107,6 +109,18 @@ class Oracle:
             self.lib.oracle_segmented_scan_u32(values, offsets, nseg, values.size,
                                                int(inclusive), out)
         return out
+
+    def linear_recurrence(self, a: np.ndarray, b: np.ndarray, inclusive: bool):
+        """h[t] = a[t] h[t-1] + b[t] from h[-1] = 0.  Returns (double h, or the
+        state before each step if exclusive; double magnitude recurrence
+        g[t] = |a[t]| g[t-1] + |b[t]| over the same range)."""
+        a = np.ascontiguousarray(a, dtype=np.float32)
+        b = np.ascontiguousarray(b, dtype=np.float32)
+        assert a.size == b.size
+        y = np.empty(a.size, dtype=np.float64)
+        g = np.empty(a.size, dtype=np.float64)
+        self.lib.oracle_linear_recurrence_f32(a, b, a.size, int(inclusive), y, g)
+        return y, g
 
     def compact(self, records: np.ndarray, flags: np.ndarray):
         """records: (n, w) array of any dtype, one row per record.  Returns (out, count)

@@ -25,6 +25,8 @@
  *     scans" and "Contract": segment s is rows [offsets[s], offsets[s+1]),
  *     the running total restarts at every segment, empty segments write
  *     nothing.
+ *   - "Parallel Prefix Sum (Scan), in depth", section "What scan builds": the
+ *     first-order linear recurrence h[t] = a[t] h[t-1] + b[t].
  *
  * Readings where the pages leave a step open (each also listed in the
  * design notes):
@@ -35,6 +37,11 @@
  *     1e-4 * sum|x| + 1e-6.
  *   - segmented rows outside [offsets[0], offsets[N]) are left untouched.
  *   - compaction flags are bytes, nonzero means keep.
+ *   - linear recurrence: the state before the first step is 0 (the page's
+ *     worked example starts from it); inputs are f32, the reference runs
+ *     the loop in double; exclusive output is the state before each step;
+ *     alongside it the same recurrence on |a| and |b|, which the tests turn
+ *     into the tolerance 1e-4 * g + 1e-6.
  */
 #include <stddef.h>
 #include <stdint.h>
@@ -135,4 +142,30 @@ uint64_t oracle_compact(const void *records, const uint8_t *flags, uint64_t n,
         }
     }
     return k;
+}
+
+/*
+ * First-order linear recurrence h[t] = a[t] * h[t-1] + b[t], h[-1] = 0, as
+ * the sequential loop the definition states, in double from f32 inputs.
+ * Inclusive: y[t] = h[t].  Exclusive: y[t] = h[t-1], so y[0] = 0.
+ * mag[t] (if not NULL) runs the same loop on magnitudes over the same range:
+ * g[t] = |a[t]| * g[t-1] + |b[t]|, g[-1] = 0.
+ */
+void oracle_linear_recurrence_f32(const float *a, const float *b, uint64_t n, int inclusive,
+                                  double *y, double *mag)
+{
+    double h = 0.0, g = 0.0;
+    for (uint64_t t = 0; t < n; ++t) {
+        double at = (double)a[t], bt = (double)b[t];
+        if (!inclusive) {
+            if (y) y[t] = h;
+            if (mag) mag[t] = g;
+        }
+        h = at * h + bt;
+        g = (at < 0.0 ? -at : at) * g + (bt < 0.0 ? -bt : bt);
+        if (inclusive) {
+            if (y) y[t] = h;
+            if (mag) mag[t] = g;
+        }
+    }
 }

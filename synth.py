@@ -19,6 +19,8 @@ Workloads (one seed per workload):
                  keep flag = (u < 0.3 * 2^64)
   segmented      n=2^27, x = u & 255, segment lengths     seed 0xD3B00005
                  empty with p=0.05 else Zipf(1.2) clamped to 2^22
+  recurrence     n=2^28, a = 0.5 + (u >> 41) * 2^-24      seed 0xD3B00006
+                 (uniform in [0.5, 1)), b as f32 above     seed 0xD3B00007
 """
 from __future__ import annotations
 
@@ -36,6 +38,8 @@ SEED_U32_FULL = 0xD3B00002
 SEED_F32 = 0xD3B00003
 SEED_RECORDS = 0xD3B00004
 SEED_SEGMENTED = 0xD3B00005
+SEED_RECURRENCE_A = 0xD3B00006
+SEED_RECURRENCE_B = 0xD3B00007
 
 _CHUNK = 1 << 22
 
@@ -115,6 +119,17 @@ def f32_values(n: int, seed: int = SEED_F32) -> np.ndarray:
         c1 = min(n, c0 + _CHUNK)
         k = (u64(seed, c0, c1 - c0) >> np.uint64(40)).astype(np.float64)
         out[c0:c1] = (k * 2.0**-23 - 1.0).astype(np.float32)
+    return out
+
+
+def decay_values(n: int, seed: int = SEED_RECURRENCE_A, lo: float = 0.5) -> np.ndarray:
+    """Floats uniform on the 2^-24 grid of [lo, lo + 0.5) (lo = 0.5: [0.5, 1)),
+    exactly representable in f32 for lo in {-1, -0.5, 0.5}."""
+    out = np.empty(n, dtype=np.float32)
+    for c0 in range(0, n, _CHUNK):
+        c1 = min(n, c0 + _CHUNK)
+        k = (u64(seed, c0, c1 - c0) >> np.uint64(41)).astype(np.float64)
+        out[c0:c1] = (lo + k * 2.0**-24).astype(np.float32)
     return out
 
 

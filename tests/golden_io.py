@@ -17,6 +17,6 @@ def load(name: str = "worked_examples.ini") -> dict:
             elif k in ("total", "count"):
                 d[k] = int(v)
             else:
-                d[k] = [int(t) for t in v.split()]
+                d[k] = [float(t) if "." in t else int(t) for t in v.split()]
         out[sec] = d
     return out

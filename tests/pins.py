@@ -14,7 +14,10 @@ Independent references used here:
   * a Hillis-Steele step simulation and a Blelloch up/down-sweep written from
     the descriptions in "Parallel Prefix Sum (Scan), in depth";
   * closed forms and invariants, and numpy library routines (cumsum, boolean
-    indexing, nonzero) that the oracle does not use.
+    indexing, nonzero) that the oracle does not use;
+  * for the linear recurrence, its closed-form expansion and a tree scan of
+    the (a, b) pairs under the page's pair combination, both in exact
+    rational arithmetic (fractions.Fraction) on the f32 inputs.
 """
 from __future__ import annotations
 
@@ -310,6 +313,115 @@ def pin_compaction_properties(o):
             assert (out[k:] == 0).all(), (n, kind)
 
 
+# ----------------------------------------------------------------------------
+# pins: linear recurrence h[t] = a[t] h[t-1] + b[t], h[-1] = 0
+
+
+def _exact(v):
+    from fractions import Fraction
+    return [Fraction(float(x)) for x in v]
+
+
+def recurrence_expansion(a, b, inclusive):
+    """Each output written out on its own: the state after step s is
+    sum_{j <= s} b[j] * prod_{j < k <= s} a[k]; inclusive reports s = t,
+    exclusive s = t - 1 (the empty sum, 0, for t = 0).  Exact rationals,
+    rounded once to double."""
+    from fractions import Fraction
+    A, B = _exact(a), _exact(b)
+    out = []
+    for t in range(len(A)):
+        s = t if inclusive else t - 1
+        acc = Fraction(0)
+        for j in range(s + 1):
+            p = B[j]
+            for k in range(j + 1, s + 1):
+                p *= A[k]
+            acc += p
+        out.append(float(acc))
+    return out
+
+
+def pair_tree_scan(a, b):
+    """Inclusive scan of the pairs under the page's combination, (a1, b1) then
+    (a2, b2) = (a1 a2, a2 b1 + b2), evaluated as a Hillis-Steele tree (in step
+    d every element combines with the one d places to its left, reading the
+    previous step), exact rationals.  The b part of pair t is h[t]."""
+    cur = list(zip(_exact(a), _exact(b)))
+    d = 1
+    while d < len(cur):
+        nxt = list(cur)
+        for i in range(d, len(cur)):
+            (a1, b1), (a2, b2) = cur[i - d], cur[i]
+            nxt[i] = (a1 * a2, a2 * b1 + b2)
+        cur = nxt
+        d *= 2
+    return [float(y) for _, y in cur]
+
+
+def pin_recurrence_golden(o):
+    """The printed example: a = [0.5, 0.9, 0.1, 1.0], b = [1, 2, 3, 4] gives
+    [1.0, 2.9, 3.29, 7.29] by the loop and by the pair scan.  The inputs are
+    f32 (0.9 and 0.1 are not exact), so agreement is to f32 input rounding."""
+    ex = GOLD["linear_recurrence"]
+    a, b = np.array(ex["a"], np.float32), np.array(ex["b"], np.float32)
+    want = np.array(ex["h"], np.float64)
+    y, g = o.linear_recurrence(a, b, True)
+    assert (np.abs(y - want) <= 1e-6 * g).all(), y
+    assert (np.abs(np.array(pair_tree_scan(a, b)) - want) <= 1e-6 * g).all()
+    ye, _ = o.linear_recurrence(a, b, False)
+    assert ye[0] == 0.0 and (np.abs(ye[1:] - want[:-1]) <= 1e-6 * g[:-1]).all()
+
+
+def pin_recurrence_expansion(o):
+    """n = 0 .. 12, 31, 32, 33, 40 with signed a in [-1.5, 1.5) and b in [-1, 1):
+    the oracle equals the closed-form expansion and the pair tree scan to
+    double rounding, in both modes; its magnitude output equals the expansion
+    on |a| and |b|."""
+    for n in list(range(0, 13)) + [31, 32, 33, 40]:
+        a = (synth.f32_values(n, seed=9000 + n) * np.float32(1.5)).astype(np.float32)
+        b = synth.f32_values(n, seed=9100 + n)
+        for inc in (False, True):
+            y, g = o.linear_recurrence(a, b, inc)
+            ref = np.array(recurrence_expansion(a, b, inc))
+            mag = np.array(recurrence_expansion(np.abs(a), np.abs(b), inc))
+            assert (np.abs(y - ref) <= 1e-12 * (mag + 1.0)).all(), (n, inc)
+            assert (np.abs(g - mag) <= 1e-12 * (mag + 1.0)).all(), (n, inc)
+        tree = np.array(pair_tree_scan(a, b))
+        assert (tree == np.array(recurrence_expansion(a, b, True))).all(), n
+
+
+def pin_recurrence_special_cases(o):
+    """a = 1: the running sum of b (numpy's sequential double cumsum, bit for
+    bit); a = 0: h = b; b = 0: h = 0; a = c, b = 1: the geometric series
+    (1 - c^(t+1)) / (1 - c); a, b >= 0: magnitude = h; exclusive = inclusive
+    shifted by one, starting at 0; empty input."""
+    n = 20000
+    b = synth.f32_values(n, seed=9200)
+    ones, zeros = np.ones(n, np.float32), np.zeros(n, np.float32)
+    y, g = o.linear_recurrence(ones, b, True)
+    assert (y == np.cumsum(b.astype(np.float64))).all()
+    assert (g == np.cumsum(np.abs(b.astype(np.float64)))).all()
+    assert (o.linear_recurrence(zeros, b, True)[0] == b.astype(np.float64)).all()
+    assert (o.linear_recurrence(synth.decay_values(n, seed=9201), zeros, True)[0] == 0.0).all()
+    c = 0.75
+    y, _ = o.linear_recurrence(np.full(n, c, np.float32), ones, True)
+    t = np.arange(n, dtype=np.float64)
+    assert np.allclose(y, (1.0 - c ** (t + 1.0)) / (1.0 - c), rtol=1e-12, atol=0.0)
+    a = synth.decay_values(n, seed=9202)
+    bp = np.abs(b)
+    y, g = o.linear_recurrence(a, bp, True)
+    assert (y == g).all()
+    a = (synth.f32_values(n, seed=9203) * np.float32(1.1)).astype(np.float32)
+    for arr_b in (b, bp):
+        yi, gi = o.linear_recurrence(a, arr_b, True)
+        ye, ge = o.linear_recurrence(a, arr_b, False)
+        assert ye[0] == 0.0 and ge[0] == 0.0
+        assert (ye[1:] == yi[:-1]).all() and (ge[1:] == gi[:-1]).all()
+    y, g = o.linear_recurrence(np.zeros(0, np.float32), np.zeros(0, np.float32), True)
+    assert y.size == 0 and g.size == 0
+
+
 ALL_PINS = [
     pin_golden_scans,
     pin_hillis_steele_trace,
@@ -323,4 +435,7 @@ ALL_PINS = [
     pin_segmented_zipf,
     pin_compaction_golden,
     pin_compaction_properties,
+    pin_recurrence_golden,
+    pin_recurrence_expansion,
+    pin_recurrence_special_cases,
 ]

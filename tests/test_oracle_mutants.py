@@ -37,6 +37,16 @@ MUTANTS = {
     "compact_inverted_flag": ("if (flags[i] != 0) {", "if (flags[i] == 0) {"),
     "compact_wrong_source_index": ("src + i * record_bytes", "src + (i ? i - 1 : 0) * record_bytes"),
     "compact_count_dropped": ("            ++k;\n", "            k = 1;\n"),
+    "recurrence_a_index_shifted": ("double at = (double)a[t], bt = (double)b[t];",
+                                   "double at = (double)a[t ? t - 1 : 0], bt = (double)b[t];"),
+    "recurrence_initial_state_one": ("double h = 0.0, g = 0.0;", "double h = 1.0, g = 0.0;"),
+    "recurrence_roles_swapped": ("h = at * h + bt;", "h = bt * h + at;"),
+    "recurrence_dropped_coefficient": ("h = at * h + bt;", "h = h + bt;"),
+    "recurrence_magnitude_lost_abs": ("g = (at < 0.0 ? -at : at) * g + (bt < 0.0 ? -bt : bt);",
+                                      "g = at * g + bt;"),
+    "recurrence_exclusive_after_step": ("        if (!inclusive) {\n            if (y) y[t] = h;",
+                                        "        if (!inclusive) {\n            if (y) y[t] = at * h + bt;"),
+    "recurrence_float_state": ("double h = 0.0, g = 0.0;", "float h = 0.0f; double g = 0.0;"),
 }
 
 
