@@ -200,7 +200,7 @@ def main() -> None:
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=10.0)
-    ap.add_argument("--only", default=None, choices=["segscan", "compact"],
+    ap.add_argument("--only", default=None, choices=["segscan", "compact", "recurrence"],
                     help="time only this workload (at --log2n) and print its entry; for "
                          "profiler captures")
     ap.add_argument("--log2n", type=int, default=28,
@@ -409,6 +409,7 @@ def measure_secondary(dwp, lib, dev, stream, peaks, x, y, scratch, need) -> dict
     out["fallback_one_silent_tile"] = measure_fallback(dwp, lib, stream, x, y, scratch, need)
     out["segscan_u32_exclusive"] = measure_segscan(dwp, lib, dev, stream, peaks)
     out["compact_16B_records"] = measure_compact(dwp, lib, dev, stream, peaks)
+    out["linear_recurrence_f32"] = measure_recurrence(dwp, lib, dev, stream, peaks)
     return out
 
 
@@ -462,7 +463,8 @@ def run_only(args) -> None:
     dev = torch.device("cuda", 0)
     lib = dwp.load()
     stream = torch.cuda.current_stream(dev)
-    fn = measure_segscan if args.only == "segscan" else measure_compact
+    fn = {"segscan": measure_segscan, "compact": measure_compact,
+          "recurrence": measure_recurrence}[args.only]
     r = fn(dwp, lib, dev, stream, measured_peaks(), log2n=args.log2n, steps=args.steps,
            warmup=args.warmup)
     print(json.dumps({"only": args.only, **r}), flush=True)
@@ -523,6 +525,33 @@ def measure_segscan(dwp, lib, dev, stream, peaks, log2n=27, steps=200, warmup=5)
             "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": alg,
             "workload": ("segmented exclusive u32 sum scan, n=2^%d values in [0,255], Zipf(1.2) " % log2n) +
                         "lengths capped at 2^22, 5% empty, CSR offsets (SplitMix64 seed 0xD3B00005)"}
+
+
+def measure_recurrence(dwp, lib, dev, stream, peaks, log2n=28, steps=200, warmup=5) -> dict:
+    """f32 linear recurrence h[t] = a[t] h[t-1] + b[t], inclusive, n = 2^28,
+    a uniform in [0.5, 1), b uniform in [-1, 1)."""
+    import ctypes
+    import torch
+    n = 1 << log2n
+    a = torch.from_numpy(synth.decay_values(n)).to(dev)
+    b = torch.from_numpy(synth.f32_values(n, seed=synth.SEED_RECURRENCE_B)).to(dev)
+    h = torch.empty_like(b)
+    need = dwp.linear_recurrence_scratch_bytes(n)
+    scratch = dwp.alloc_scratch(need, dev)
+    sb = ctypes.c_size_t(need)
+    args = (ctypes.c_void_p(a.data_ptr()), ctypes.c_void_p(b.data_ptr()), ctypes.c_void_p(h.data_ptr()),
+            n, dwp.DWP_INCLUSIVE, ctypes.c_void_p(scratch.data_ptr()), ctypes.byref(sb),
+            ctypes.c_void_p(int(stream.cuda_stream)))
+    ms = time_calls(lambda: lib.dwp_linear_recurrence_f32(*args), steps, warmup, stream)
+    if dwp.read_status(scratch) != dwp.DWP_SUCCESS:
+        raise RuntimeError("linear recurrence reported a device-side error")
+    alg = 12 * n
+    gbs = alg / (ms * 1e-3) / 1e9
+    return {"n": n, "ms": ms, "Gelem_s": n / (ms * 1e-3) / 1e9, "GB_s": gbs,
+            "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": alg,
+            "workload": "f32 linear recurrence h[t] = a[t] h[t-1] + b[t], inclusive, n=2^%d, "
+                        "a uniform in [0.5,1), b uniform in [-1,1) (SplitMix64 seeds 0xD3B00006/7)"
+                        % log2n}
 
 
 if __name__ == "__main__":

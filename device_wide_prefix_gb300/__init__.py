@@ -44,6 +44,7 @@ EXPORTS = [
     "dwp_scan_inclusive",
     "dwp_segmented_scan_u32",
     "dwp_compact_by_flags",
+    "dwp_linear_recurrence_f32",
     "dwp_read_status",
     "dwp_read_fallbacks",
     "dwp_status_string",
@@ -81,6 +82,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dwp_segmented_scan_u32.restype = c.c_int
     lib.dwp_compact_by_flags.argtypes = [P, P, S, P, P, P, Z, P]
     lib.dwp_compact_by_flags.restype = c.c_int
+    lib.dwp_linear_recurrence_f32.argtypes = [P, P, P, S, c.c_int, P, Z, P]
+    lib.dwp_linear_recurrence_f32.restype = c.c_int
     lib.dwp_read_status.argtypes = [P, P]
     lib.dwp_read_status.restype = c.c_int
     lib.dwp_read_fallbacks.argtypes = [P, P, c.POINTER(c.c_uint32)]
@@ -126,6 +129,14 @@ def dwp_segmented_scan_u32(d_values, d_offsets, num_segments, d_out, n, mode, d_
     st = load().dwp_segmented_scan_u32(d_values or None, d_offsets or None, num_segments,
                                        d_out or None, n, int(mode), d_scratch or None,
                                        ctypes.byref(sb), stream or None)
+    return st, sb.value
+
+
+def dwp_linear_recurrence_f32(d_a, d_b, d_h, n, mode, d_scratch, scratch_bytes, stream):
+    """dwp.h dwp_linear_recurrence_f32; returns (status, scratch_bytes after the call)."""
+    sb = ctypes.c_size_t(scratch_bytes)
+    st = load().dwp_linear_recurrence_f32(d_a or None, d_b or None, d_h or None, n, int(mode),
+                                          d_scratch or None, ctypes.byref(sb), stream or None)
     return st, sb.value
 
 
@@ -273,6 +284,35 @@ def segmented_scan(values, offsets, inclusive: bool = False, out=None, scratch=N
                                        DWP_INCLUSIVE if inclusive else DWP_EXCLUSIVE,
                                        scratch.data_ptr(), scratch.numel(), _stream_of(values, stream))
     _check(st, "dwp_segmented_scan_u32")
+    return out
+
+
+def linear_recurrence_scratch_bytes(n: int) -> int:
+    st, b = dwp_linear_recurrence_f32(None, None, None, n, DWP_INCLUSIVE, None, 0, None)
+    _check(st, "linear recurrence scratch size query")
+    return b
+
+
+def linear_recurrence(a, b, inclusive: bool = True, out=None, scratch=None, stream=None):
+    """h[t] = a[t] h[t-1] + b[t] from h[-1] = 0 over contiguous CUDA float32
+    tensors `a` and `b` of equal length.  Inclusive returns h; exclusive the
+    state before each step.  `out` may be `a` or `b` itself (in place)."""
+    torch = _torch()
+    if not (a.is_cuda and b.is_cuda and a.is_contiguous() and b.is_contiguous()):
+        raise ValueError("a and b must be contiguous CUDA tensors")
+    if a.dtype != torch.float32 or b.dtype != torch.float32 or a.numel() != b.numel():
+        raise ValueError("a and b must be float32 tensors of the same length")
+    n = a.numel()
+    if out is None:
+        out = torch.empty_like(b)
+    need = linear_recurrence_scratch_bytes(n)
+    if scratch is None:
+        scratch = alloc_scratch(need, a.device)
+    with torch.cuda.device(a.device):
+        st, _ = dwp_linear_recurrence_f32(a.data_ptr(), b.data_ptr(), out.data_ptr(), n,
+                                          DWP_INCLUSIVE if inclusive else DWP_EXCLUSIVE,
+                                          scratch.data_ptr(), scratch.numel(), _stream_of(a, stream))
+    _check(st, "dwp_linear_recurrence_f32")
     return out
 
 

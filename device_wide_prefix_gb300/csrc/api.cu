@@ -142,6 +142,43 @@ dwp_status compact_common(const void *records, const uint8_t *flags, size_t n, v
     return DWP_SUCCESS;
 }
 
+dwp_status recurrence_common(const float *a, const float *b, float *h, size_t n, dwp_mode mode,
+                             void *scratch, size_t *scratch_bytes, dwp_stream stream) {
+    if (!scratch_bytes) return DWP_ERR_INVALID_VALUE;
+    const int m = static_cast<int>(mode);
+    if (m != DWP_EXCLUSIVE && m != DWP_INCLUSIVE) return DWP_ERR_INVALID_VALUE;
+    if (uint64_t(n) > kMaxN) return DWP_ERR_INVALID_VALUE;
+    const uint64_t tiles = ceil_div(n, recurrence_tile_elems());
+    const size_t need = kHeaderBytes + 16u * tiles;  // two descriptor words per tile
+    if (!scratch) {
+        *scratch_bytes = need;
+        return DWP_SUCCESS;
+    }
+    if (*scratch_bytes < need) return DWP_ERR_SCRATCH_TOO_SMALL;
+    if (n > 0 && (!a || !b || !h)) return DWP_ERR_INVALID_VALUE;
+    if (!aligned16(scratch) || (n > 0 && (!aligned16(a) || !aligned16(b) || !aligned16(h))))
+        return DWP_ERR_MISALIGNED;
+    const uint64_t bytes = uint64_t(n) * 4u;
+    // h may be a or b exactly (in place); a partial overlap is rejected
+    if ((h != a && overlap(h, bytes, a, bytes)) || (h != b && overlap(h, bytes, b, bytes)))
+        return DWP_ERR_ALIASING;
+    if (overlap(scratch, need, a, bytes) || overlap(scratch, need, b, bytes) ||
+        overlap(scratch, need, h, bytes))
+        return DWP_ERR_ALIASING;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(scratch, 0, need, s) != cudaSuccess) {
+        cudaGetLastError();
+        return DWP_ERR_CUDA;
+    }
+    if (n == 0) return DWP_SUCCESS;
+    if (launch_recurrence(a, b, h, n, m == DWP_INCLUSIVE, scratch, s) != cudaSuccess) {
+        cudaGetLastError();
+        return DWP_ERR_CUDA;
+    }
+    return DWP_SUCCESS;
+}
+
 }  // namespace
 
 extern "C" {
@@ -167,6 +204,12 @@ dwp_status dwp_scan_exclusive(dwp_op op, const void *d_in, void *d_out, size_t n
 dwp_status dwp_scan_inclusive(dwp_op op, const void *d_in, void *d_out, size_t n,
                               void *d_scratch, size_t *scratch_bytes, dwp_stream stream) {
     return scan_common(true, op, d_in, d_out, n, d_scratch, scratch_bytes, stream);
+}
+
+dwp_status dwp_linear_recurrence_f32(const float *d_a, const float *d_b, float *d_h, size_t n,
+                                     dwp_mode mode, void *d_scratch, size_t *scratch_bytes,
+                                     dwp_stream stream) {
+    return recurrence_common(d_a, d_b, d_h, n, mode, d_scratch, scratch_bytes, stream);
 }
 
 dwp_status dwp_read_status(const void *d_scratch, dwp_stream stream) {

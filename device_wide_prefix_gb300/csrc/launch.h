@@ -32,4 +32,11 @@ uint32_t compact_tile_records();
 cudaError_t launch_compact(const void *records, const uint8_t *flags, uint64_t n, void *out,
                            uint32_t *count, void *scratch, cudaStream_t stream);
 
+// Elements per tile of the linear-recurrence kernel.
+uint32_t recurrence_tile_elems();
+// One launch of the f32 linear recurrence h[t] = a[t] h[t-1] + b[t]
+// (scratch already cleared: header + 16 bytes per tile; n >= 1).
+cudaError_t launch_recurrence(const float *a, const float *b, float *h, uint64_t n, bool inclusive,
+                              void *scratch, cudaStream_t stream);
+
 }  // namespace dwp

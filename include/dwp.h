@@ -186,6 +186,29 @@ dwp_status dwp_scan_static_scratch(dwp_op op, dwp_mode mode, const void *d_in, v
                                    size_t n, dwp_stream stream);
 
 /*
+ * First-order linear recurrence ("Parallel Prefix Sum (Scan), in depth",
+ * section "What scan builds"): h[t] = a[t] * h[t-1] + b[t] with h[-1] = 0,
+ * computed as a single-pass scan of the pairs (a[t], b[t]) under
+ * (a1, b1) then (a2, b2) = (a1 a2, a2 b1 + b2).
+ *   d_a, d_b  n f32 coefficients and inputs (device, 16-byte aligned).
+ *   d_h       n f32 outputs (device, 16-byte aligned).  DWP_INCLUSIVE
+ *             writes h[t]; DWP_EXCLUSIVE writes the state before step t,
+ *             h[t-1] (0 at t = 0).  d_h may equal d_a or d_b exactly (in
+ *             place); any other overlap with them is DWP_ERR_ALIASING.
+ *   d_scratch NULL: *scratch_bytes receives the size needed (a 128-byte
+ *             header plus 16 bytes per tile) and nothing else happens.
+ *             Otherwise at least that many bytes, 16-byte aligned, owned by
+ *             the caller, overlapping no other argument.
+ * Arithmetic is f32 with one fused multiply-add per step; the grouping
+ * differs from the sequential loop, so results agree with it to f32
+ * rounding, not bit for bit.  Errors as for dwp_scan_exclusive; the
+ * Decoupled Fallback applies except in place.
+ */
+dwp_status dwp_linear_recurrence_f32(const float *d_a, const float *d_b, float *d_h, size_t n,
+                                     dwp_mode mode, void *d_scratch, size_t *scratch_bytes,
+                                     dwp_stream stream);
+
+/*
  * Device-side status of the most recent call that used d_scratch.
  * Synchronises `stream`, then reads the status word.  Returns DWP_SUCCESS,
  * DWP_ERR_LOOKBACK_TIMEOUT or DWP_ERR_PIPELINE_TIMEOUT; DWP_ERR_CUDA if the

@@ -111,3 +111,44 @@ def test_null_scratch_bytes_pointer(lib):
     assert lib.dwp_read_fallbacks(None, None, ctypes.byref(v)) == dwp.DWP_ERR_INVALID_VALUE
     assert lib.dwp_read_fallbacks(ctypes.c_void_p(4096), None, None) == dwp.DWP_ERR_INVALID_VALUE
     assert v.value == 7
+
+
+def test_recurrence_size_query_and_validation(lib):
+    R = dwp.dwp_linear_recurrence_f32
+    st, b0 = R(0, 0, 0, 0, dwp.DWP_INCLUSIVE, 0, 0, 0)
+    assert st == dwp.DWP_SUCCESS and b0 == 128
+    _, b1 = R(0, 0, 0, 1, dwp.DWP_INCLUSIVE, 0, 0, 0)
+    assert b1 == 128 + 16  # two descriptor words per tile
+    T = 1
+    while R(0, 0, 0, 2 * T, dwp.DWP_INCLUSIVE, 0, 0, 0)[1] == b1:
+        T *= 2
+    lo, hi = T, 2 * T
+    while hi - lo > 1:
+        mid = (lo + hi) // 2
+        if R(0, 0, 0, mid, dwp.DWP_INCLUSIVE, 0, 0, 0)[1] == b1:
+            lo = mid
+        else:
+            hi = mid
+    T = lo
+    for k in (1, 9, 1000):
+        assert R(0, 0, 0, k * T, dwp.DWP_EXCLUSIVE, 0, 0, 0)[1] == 128 + 16 * k
+        assert R(0, 0, 0, k * T + 1, dwp.DWP_EXCLUSIVE, 0, 0, 0)[1] == 128 + 16 * (k + 1)
+    n = 1000
+    need = R(0, 0, 0, n, dwp.DWP_INCLUSIVE, 0, 0, 0)[1]
+    a, b, h, s = A, A + 8192, A + 16384, A + (1 << 30)
+    ok = dwp.DWP_INCLUSIVE
+    assert R(a, b, h, n, 2, s, need, 0)[0] == dwp.DWP_ERR_INVALID_VALUE
+    assert R(a, b, h, 1 << 32, ok, s, need, 0)[0] == dwp.DWP_ERR_INVALID_VALUE
+    assert R(a, b, h, n, ok, s, need - 1, 0)[0] == dwp.DWP_ERR_SCRATCH_TOO_SMALL
+    assert R(0, b, h, n, ok, s, need, 0)[0] == dwp.DWP_ERR_INVALID_VALUE
+    assert R(a, 0, h, n, ok, s, need, 0)[0] == dwp.DWP_ERR_INVALID_VALUE
+    assert R(a, b, 0, n, ok, s, need, 0)[0] == dwp.DWP_ERR_INVALID_VALUE
+    assert R(a + 4, b, h, n, ok, s, need, 0)[0] == dwp.DWP_ERR_MISALIGNED
+    assert R(a, b + 8, h, n, ok, s, need, 0)[0] == dwp.DWP_ERR_MISALIGNED
+    assert R(a, b, h + 12, n, ok, s, need, 0)[0] == dwp.DWP_ERR_MISALIGNED
+    assert R(a, b, h, n, ok, s + 8, need, 0)[0] == dwp.DWP_ERR_MISALIGNED
+    assert R(a, b, b + 16, n, ok, s, need, 0)[0] == dwp.DWP_ERR_ALIASING   # h overlaps b partly
+    assert R(a, b, a + 32, n, ok, s, need, 0)[0] == dwp.DWP_ERR_ALIASING   # h overlaps a partly
+    assert R(a, b, h, n, ok, h + 16, need, 0)[0] == dwp.DWP_ERR_ALIASING   # scratch over h
+    import ctypes
+    assert lib.dwp_linear_recurrence_f32(None, None, None, 10, 1, None, None, None) == dwp.DWP_ERR_INVALID_VALUE
