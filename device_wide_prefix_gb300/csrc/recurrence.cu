@@ -80,22 +80,22 @@ struct RecConfig {
 };
 
 #ifndef DWP_REC_WARPS
-#define DWP_REC_WARPS 8
+#define DWP_REC_WARPS 4
 #endif
 #ifndef DWP_REC_ITEMS
-#define DWP_REC_ITEMS 12
+#define DWP_REC_ITEMS 36
 #endif
 #ifndef DWP_REC_IN
 #define DWP_REC_IN 2
 #endif
 #ifndef DWP_REC_OUT
-#define DWP_REC_OUT 4
+#define DWP_REC_OUT 3
 #endif
 #ifndef DWP_REC_RING
 #define DWP_REC_RING 16
 #endif
 #ifndef DWP_REC_LOOKERS
-#define DWP_REC_LOOKERS 16
+#define DWP_REC_LOOKERS 4
 #endif
 #ifndef DWP_REC_AHEAD
 #define DWP_REC_AHEAD 2
