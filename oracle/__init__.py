@@ -58,6 +58,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.oracle_compact.restype = c.c_uint64
     lib.oracle_linear_recurrence_f32.argtypes = [_f32p, _f32p, c.c_uint64, c.c_int, _f64p, _f64p]
     lib.oracle_linear_recurrence_f32.restype = None
+    lib.oracle_segmented_reduce_u32.argtypes = [_u32p, _u32p, c.c_uint64, c.c_uint64, _u32p]
+    lib.oracle_segmented_reduce_u32.restype = None
     if path is None:
         _lib = lib
     return lib
@@ -108,6 +110,16 @@ class Oracle:
         if nseg:
             self.lib.oracle_segmented_scan_u32(values, offsets, nseg, values.size,
                                                int(inclusive), out)
+        return out
+
+    def segmented_reduce_u32(self, values: np.ndarray, offsets: np.ndarray) -> np.ndarray:
+        """One wrapping u32 sum per segment of the CSR offsets (0 if empty)."""
+        values = np.ascontiguousarray(values, dtype=np.uint32)
+        offsets = np.ascontiguousarray(offsets, dtype=np.uint32)
+        nseg = max(offsets.size - 1, 0)
+        out = np.empty(nseg, dtype=np.uint32)
+        if nseg:
+            self.lib.oracle_segmented_reduce_u32(values, offsets, nseg, values.size, out)
         return out
 
     def linear_recurrence(self, a: np.ndarray, b: np.ndarray, inclusive: bool):

@@ -27,6 +27,9 @@
  *     nothing.
  *   - "Parallel Prefix Sum (Scan), in depth", section "What scan builds": the
  *     first-order linear recurrence h[t] = a[t] h[t-1] + b[t].
+ *   - "GPUSegmentedScan" (luma.gl), section "Composition": the segmented
+ *     reduction it names beside the segmented scan, read as one u32 sum per
+ *     segment of the same CSR offsets.
  *
  * Readings where the pages leave a step open (each also listed in the
  * design notes):
@@ -37,6 +40,8 @@
  *     1e-4 * sum|x| + 1e-6.
  *   - segmented rows outside [offsets[0], offsets[N]) are left untouched.
  *   - compaction flags are bytes, nonzero means keep.
+ *   - segmented reduction: out[s] is the wrapping u32 sum of rows
+ *     [offsets[s], offsets[s+1]); an empty segment gives 0, the identity.
  *   - linear recurrence: the state before the first step is 0 (the page's
  *     worked example starts from it); inputs are f32, the reference runs
  *     the loop in double; exclusive output is the state before each step;
@@ -167,5 +172,26 @@ void oracle_linear_recurrence_f32(const float *a, const float *b, uint64_t n, in
             if (y) y[t] = h;
             if (mag) mag[t] = g;
         }
+    }
+}
+
+/*
+ * Segmented u32 addition reduction over CSR offsets (num_segments + 1
+ * entries): out[s] = values[offsets[s]] + ... + values[offsets[s+1] - 1],
+ * wrapping modulo 2^32, and 0 for an empty segment.  Offsets are assumed
+ * non-decreasing with offsets[num_segments] <= n; the loop clamps to n so
+ * that a broken precondition cannot read out of range.
+ */
+void oracle_segmented_reduce_u32(const uint32_t *values, const uint32_t *offsets,
+                                 uint64_t num_segments, uint64_t n, uint32_t *out)
+{
+    for (uint64_t s = 0; s < num_segments; ++s) {
+        uint64_t first = offsets[s], end = offsets[s + 1];
+        if (end > n)
+            end = n;
+        uint32_t acc = 0u;
+        for (uint64_t i = first; i < end; ++i)
+            acc = acc + values[i];
+        out[s] = acc;
     }
 }

@@ -274,6 +274,70 @@ def pin_segmented_zipf(o):
 
 
 # ----------------------------------------------------------------------------
+# pins: segmented reduction
+
+
+def _reduce_ref(values, offsets):
+    """numpy: uint64 reduceat per non-empty segment, then mod 2^32; 0 for empty."""
+    nseg = len(offsets) - 1
+    out = np.zeros(nseg, np.uint64)
+    v64 = values.astype(np.uint64)
+    lo = offsets[:-1].astype(np.int64)
+    hi = offsets[1:].astype(np.int64)
+    nonempty = np.nonzero(hi > lo)[0]
+    if nonempty.size:
+        sums = np.add.reduceat(v64, lo[nonempty])
+        # reduceat sums up to the next listed start; the next start of a
+        # non-empty segment is the end of it (empties are skipped), except
+        # after the last one, which runs to the end of the array
+        if hi[nonempty[-1]] < values.size:
+            sums[-1] -= np.sum(v64[hi[nonempty[-1]]:], dtype=np.uint64)
+        out[nonempty] = sums
+    return (out % 2**32).astype(np.uint32)
+
+
+def pin_segmented_reduce(o):
+    """The printed segmented example's segment totals (the last inclusive value
+    of each segment: [5, 15, 7]); numpy reduceat on the shapes of the
+    segmented pins and on the skewed generator; brute force on tiny inputs;
+    empty segments give 0; one segment gives the wrapping total; all length
+    1 gives the values; the totals add up to the covered rows' sum."""
+    ex = GOLD["segmented_luma"]
+    v = np.array(ex["values"], np.uint32)
+    off = np.array(ex["offsets"], np.uint32)
+    incl = ex["inclusive"]
+    ends = [int(off[s + 1]) - 1 for s in range(len(off) - 1)]
+    assert o.segmented_reduce_u32(v, off).tolist() == [incl[e] for e in ends] == [5, 15, 7]
+    n = 3000
+    v = synth.u32_full_values(n, seed=7200)
+    shapes = [[0, n], list(range(n + 1)), [0, 0, 0, 5, 5, 100, 100, 100, 1500, 2999, n, n, n],
+              [7, 7, 40, 1000, 2500]]
+    for offs in shapes:
+        off = np.array(offs, np.uint32)
+        got = o.segmented_reduce_u32(v, off)
+        assert (got == _reduce_ref(v, off)).all(), offs[:4]
+        assert int(np.sum(got, dtype=np.uint64)) % 2**32 == \
+            int(np.sum(v[off[0]:off[-1]], dtype=np.uint64)) % 2**32
+        empty = np.nonzero(off[1:] == off[:-1])[0]
+        assert (got[empty] == 0).all()
+    assert (o.segmented_reduce_u32(v, np.arange(n + 1, dtype=np.uint32)) == v).all()
+    assert int(o.segmented_reduce_u32(v, np.array([0, n], np.uint32))[0]) == \
+        int(np.sum(v, dtype=np.uint64)) % 2**32
+    for k in range(20):
+        m = k + 1
+        vv = synth.u32_full_values(m, seed=7300 + k)
+        cuts = np.sort(synth.u32_small_values(k % 5 + 1, seed=7400 + k) % (m + 1))
+        off = np.concatenate([[0], cuts, [m]]).astype(np.uint32)
+        want = [sum(int(vv[j]) for j in range(int(off[s]), int(off[s + 1]))) % 2**32
+                for s in range(off.size - 1)]
+        assert o.segmented_reduce_u32(vv, off).tolist() == want
+    nz = 1 << 18
+    off = synth.segment_offsets(nz, seed=7500, cap=1 << 14)
+    vz = synth.u32_byte_values(nz, seed=7501)
+    assert (o.segmented_reduce_u32(vz, off) == _reduce_ref(vz, off)).all()
+
+
+# ----------------------------------------------------------------------------
 # pins: compaction
 
 
@@ -433,6 +497,7 @@ ALL_PINS = [
     pin_segmented_golden,
     pin_segmented_shapes,
     pin_segmented_zipf,
+    pin_segmented_reduce,
     pin_compaction_golden,
     pin_compaction_properties,
     pin_recurrence_golden,

@@ -37,6 +37,13 @@ MUTANTS = {
     "compact_inverted_flag": ("if (flags[i] != 0) {", "if (flags[i] == 0) {"),
     "compact_wrong_source_index": ("src + i * record_bytes", "src + (i ? i - 1 : 0) * record_bytes"),
     "compact_count_dropped": ("            ++k;\n", "            k = 1;\n"),
+    "reduce_start_off_by_one": ("        uint32_t acc = 0u;\n        for (uint64_t i = first; i < end; ++i)\n            acc = acc + values[i];",
+                                "        uint32_t acc = 0u;\n        for (uint64_t i = first + 1; i < end; ++i)\n            acc = acc + values[i];"),
+    "reduce_end_inclusive": ("        uint32_t acc = 0u;\n        for (uint64_t i = first; i < end; ++i)\n            acc = acc + values[i];",
+                             "        uint32_t acc = 0u;\n        for (uint64_t i = first; i <= end && i < n; ++i)\n            acc = acc + values[i];"),
+    "reduce_no_reset": ("        uint32_t acc = 0u;\n        for (uint64_t i = first; i < end; ++i)\n            acc = acc + values[i];",
+                        "        static uint32_t acc;\n        for (uint64_t i = first; i < end; ++i)\n            acc = acc + values[i];"),
+    "reduce_wrong_slot": ("        out[s] = acc;", "        out[s ? s - 1 : 0] = acc;"),
     "recurrence_a_index_shifted": ("double at = (double)a[t], bt = (double)b[t];",
                                    "double at = (double)a[t ? t - 1 : 0], bt = (double)b[t];"),
     "recurrence_initial_state_one": ("double h = 0.0, g = 0.0;", "double h = 1.0, g = 0.0;"),
