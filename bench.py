@@ -200,7 +200,7 @@ def main() -> None:
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=10.0)
-    ap.add_argument("--only", default=None, choices=["segscan", "compact", "recurrence"],
+    ap.add_argument("--only", default=None, choices=["segscan", "compact", "recurrence", "segreduce"],
                     help="time only this workload (at --log2n) and print its entry; for "
                          "profiler captures")
     ap.add_argument("--log2n", type=int, default=28,
@@ -410,6 +410,7 @@ def measure_secondary(dwp, lib, dev, stream, peaks, x, y, scratch, need) -> dict
     out["segscan_u32_exclusive"] = measure_segscan(dwp, lib, dev, stream, peaks)
     out["compact_16B_records"] = measure_compact(dwp, lib, dev, stream, peaks)
     out["linear_recurrence_f32"] = measure_recurrence(dwp, lib, dev, stream, peaks)
+    out["segreduce_u32"] = measure_segreduce(dwp, lib, dev, stream, peaks)
     return out
 
 
@@ -464,7 +465,7 @@ def run_only(args) -> None:
     lib = dwp.load()
     stream = torch.cuda.current_stream(dev)
     fn = {"segscan": measure_segscan, "compact": measure_compact,
-          "recurrence": measure_recurrence}[args.only]
+          "recurrence": measure_recurrence, "segreduce": measure_segreduce}[args.only]
     r = fn(dwp, lib, dev, stream, measured_peaks(), log2n=args.log2n, steps=args.steps,
            warmup=args.warmup)
     print(json.dumps({"only": args.only, **r}), flush=True)
@@ -524,6 +525,34 @@ def measure_segscan(dwp, lib, dev, stream, peaks, log2n=27, steps=200, warmup=5)
     return {"n": n, "segments": nseg, "ms": ms, "Gelem_s": n / (ms * 1e-3) / 1e9, "GB_s": gbs,
             "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": alg,
             "workload": ("segmented exclusive u32 sum scan, n=2^%d values in [0,255], Zipf(1.2) " % log2n) +
+                        "lengths capped at 2^22, 5% empty, CSR offsets (SplitMix64 seed 0xD3B00005)"}
+
+
+def measure_segreduce(dwp, lib, dev, stream, peaks, log2n=27, steps=200, warmup=5) -> dict:
+    """Segmented u32 reduction over the segmented scan's skewed offsets: n = 2^27
+    values in [0, 255], Zipf(1.2) lengths capped at 2^22, 5% empty."""
+    import ctypes
+    import torch
+    n = 1 << log2n
+    off_np = synth.segment_offsets(n)
+    nseg = off_np.size - 1
+    v = torch.from_numpy(synth.u32_byte_values(n).view(np.int32)).to(dev)
+    off = torch.from_numpy(off_np.view(np.int32)).to(dev)
+    out = torch.empty(nseg, dtype=torch.int32, device=dev)
+    need = dwp.segmented_reduce_scratch_bytes(n)
+    scratch = dwp.alloc_scratch(need, dev)
+    sb = ctypes.c_size_t(need)
+    args = (ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(off.data_ptr()), nseg,
+            ctypes.c_void_p(out.data_ptr()), n, ctypes.c_void_p(scratch.data_ptr()), ctypes.byref(sb),
+            ctypes.c_void_p(int(stream.cuda_stream)))
+    ms = time_calls(lambda: lib.dwp_segmented_reduce_u32(*args), steps, warmup, stream)
+    if dwp.read_status(scratch) != dwp.DWP_SUCCESS:
+        raise RuntimeError("segmented reduction reported a device-side error")
+    alg = 4 * n + 4 * (nseg + 1) + 4 * nseg
+    gbs = alg / (ms * 1e-3) / 1e9
+    return {"n": n, "segments": nseg, "ms": ms, "Gelem_s": n / (ms * 1e-3) / 1e9, "GB_s": gbs,
+            "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": alg,
+            "workload": ("segmented u32 sum reduction, n=2^%d values in [0,255], Zipf(1.2) " % log2n) +
                         "lengths capped at 2^22, 5% empty, CSR offsets (SplitMix64 seed 0xD3B00005)"}
 
 

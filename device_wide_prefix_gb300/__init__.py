@@ -45,6 +45,7 @@ EXPORTS = [
     "dwp_segmented_scan_u32",
     "dwp_compact_by_flags",
     "dwp_linear_recurrence_f32",
+    "dwp_segmented_reduce_u32",
     "dwp_read_status",
     "dwp_read_fallbacks",
     "dwp_status_string",
@@ -84,6 +85,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dwp_compact_by_flags.restype = c.c_int
     lib.dwp_linear_recurrence_f32.argtypes = [P, P, P, S, c.c_int, P, Z, P]
     lib.dwp_linear_recurrence_f32.restype = c.c_int
+    lib.dwp_segmented_reduce_u32.argtypes = [P, P, S, P, S, P, Z, P]
+    lib.dwp_segmented_reduce_u32.restype = c.c_int
     lib.dwp_read_status.argtypes = [P, P]
     lib.dwp_read_status.restype = c.c_int
     lib.dwp_read_fallbacks.argtypes = [P, P, c.POINTER(c.c_uint32)]
@@ -129,6 +132,16 @@ def dwp_segmented_scan_u32(d_values, d_offsets, num_segments, d_out, n, mode, d_
     st = load().dwp_segmented_scan_u32(d_values or None, d_offsets or None, num_segments,
                                        d_out or None, n, int(mode), d_scratch or None,
                                        ctypes.byref(sb), stream or None)
+    return st, sb.value
+
+
+def dwp_segmented_reduce_u32(d_values, d_offsets, num_segments, d_out, n, d_scratch,
+                             scratch_bytes, stream):
+    """dwp.h dwp_segmented_reduce_u32; returns (status, scratch_bytes after the call)."""
+    sb = ctypes.c_size_t(scratch_bytes)
+    st = load().dwp_segmented_reduce_u32(d_values or None, d_offsets or None, num_segments,
+                                         d_out or None, n, d_scratch or None, ctypes.byref(sb),
+                                         stream or None)
     return st, sb.value
 
 
@@ -284,6 +297,37 @@ def segmented_scan(values, offsets, inclusive: bool = False, out=None, scratch=N
                                        DWP_INCLUSIVE if inclusive else DWP_EXCLUSIVE,
                                        scratch.data_ptr(), scratch.numel(), _stream_of(values, stream))
     _check(st, "dwp_segmented_scan_u32")
+    return out
+
+
+def segmented_reduce_scratch_bytes(n: int) -> int:
+    st, b = dwp_segmented_reduce_u32(None, None, 0, None, n, None, 0, None)
+    _check(st, "segmented reduction scratch size query")
+    return b
+
+
+def segmented_reduce(values, offsets, out=None, scratch=None, stream=None):
+    """One wrapping u32 sum per segment of CSR `offsets` (CUDA, N+1 entries)
+    over `values` (CUDA int32/uint32 bits); 0 for an empty segment.  Returns
+    `out` (N int32 entries, the u32 bits)."""
+    torch = _torch()
+    if not (values.is_cuda and offsets.is_cuda and values.is_contiguous() and offsets.is_contiguous()):
+        raise ValueError("values and offsets must be contiguous CUDA tensors")
+    if values.element_size() != 4 or offsets.element_size() != 4:
+        raise ValueError("values and offsets must have 4-byte elements")
+    n = values.numel()
+    nseg = max(offsets.numel() - 1, 0)
+    if out is None:
+        out = torch.empty(nseg, dtype=torch.int32, device=values.device)
+    need = segmented_reduce_scratch_bytes(n)
+    if scratch is None:
+        scratch = alloc_scratch(need, values.device)
+    with torch.cuda.device(values.device):
+        st, _ = dwp_segmented_reduce_u32(values.data_ptr() if n else 0,
+                                         offsets.data_ptr() if offsets.numel() else 0, nseg,
+                                         out.data_ptr() if nseg else 0, n, scratch.data_ptr(),
+                                         scratch.numel(), _stream_of(values, stream))
+    _check(st, "dwp_segmented_reduce_u32")
     return out
 
 

@@ -142,6 +142,43 @@ dwp_status compact_common(const void *records, const uint8_t *flags, size_t n, v
     return DWP_SUCCESS;
 }
 
+dwp_status segreduce_common(const uint32_t *values, const uint32_t *offsets, size_t nseg,
+                            uint32_t *out, size_t n, void *scratch, size_t *scratch_bytes,
+                            dwp_stream stream) {
+    if (!scratch_bytes) return DWP_ERR_INVALID_VALUE;
+    if (uint64_t(n) > kMaxN || uint64_t(nseg) >= kMaxN) return DWP_ERR_INVALID_VALUE;
+    const size_t need = kHeaderBytes;  // tile counter and status only: no descriptors
+    if (!scratch) {
+        *scratch_bytes = need;
+        return DWP_SUCCESS;
+    }
+    if (*scratch_bytes < need) return DWP_ERR_SCRATCH_TOO_SMALL;
+    if (n > 0 && !values) return DWP_ERR_INVALID_VALUE;
+    if (nseg > 0 && (!offsets || !out)) return DWP_ERR_INVALID_VALUE;
+    if (!aligned16(scratch) || (n > 0 && !aligned16(values)) || (offsets && !aligned4(offsets)) ||
+        (out && !aligned4(out)))
+        return DWP_ERR_MISALIGNED;
+    const uint64_t vbytes = uint64_t(n) * 4u, obytes = (uint64_t(nseg) + 1u) * 4u,
+                   rbytes = uint64_t(nseg) * 4u;
+    if (overlap(out, rbytes, values, vbytes) || overlap(out, rbytes, offsets, obytes) ||
+        overlap(out, rbytes, scratch, need) || overlap(scratch, need, values, vbytes) ||
+        overlap(scratch, need, offsets, obytes))
+        return DWP_ERR_ALIASING;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(scratch, 0, need, s) != cudaSuccess ||
+        (nseg > 0 && cudaMemsetAsync(out, 0, rbytes, s) != cudaSuccess)) {
+        cudaGetLastError();
+        return DWP_ERR_CUDA;
+    }
+    if (n == 0 || nseg == 0) return DWP_SUCCESS;  // every segment empty: all zeros
+    if (launch_segreduce(values, offsets, uint32_t(nseg), out, n, scratch, s) != cudaSuccess) {
+        cudaGetLastError();
+        return DWP_ERR_CUDA;
+    }
+    return DWP_SUCCESS;
+}
+
 dwp_status recurrence_common(const float *a, const float *b, float *h, size_t n, dwp_mode mode,
                              void *scratch, size_t *scratch_bytes, dwp_stream stream) {
     if (!scratch_bytes) return DWP_ERR_INVALID_VALUE;
@@ -204,6 +241,13 @@ dwp_status dwp_scan_exclusive(dwp_op op, const void *d_in, void *d_out, size_t n
 dwp_status dwp_scan_inclusive(dwp_op op, const void *d_in, void *d_out, size_t n,
                               void *d_scratch, size_t *scratch_bytes, dwp_stream stream) {
     return scan_common(true, op, d_in, d_out, n, d_scratch, scratch_bytes, stream);
+}
+
+dwp_status dwp_segmented_reduce_u32(const uint32_t *d_values, const uint32_t *d_offsets,
+                                    size_t num_segments, uint32_t *d_out, size_t n,
+                                    void *d_scratch, size_t *scratch_bytes, dwp_stream stream) {
+    return segreduce_common(d_values, d_offsets, num_segments, d_out, n, d_scratch, scratch_bytes,
+                            stream);
 }
 
 dwp_status dwp_linear_recurrence_f32(const float *d_a, const float *d_b, float *d_h, size_t n,

@@ -32,6 +32,13 @@ uint32_t compact_tile_records();
 cudaError_t launch_compact(const void *records, const uint8_t *flags, uint64_t n, void *out,
                            uint32_t *count, void *scratch, cudaStream_t stream);
 
+// Rows per tile of the segmented reduction kernel.
+uint32_t segreduce_tile_elems();
+// One launch of the segmented u32 reduction (out already cleared, scratch
+// header cleared; nseg >= 1, n >= 1).
+cudaError_t launch_segreduce(const uint32_t *values, const uint32_t *offsets, uint32_t nseg,
+                             uint32_t *out, uint64_t n, void *scratch, cudaStream_t stream);
+
 // Elements per tile of the linear-recurrence kernel.
 uint32_t recurrence_tile_elems();
 // One launch of the f32 linear recurrence h[t] = a[t] h[t-1] + b[t]

@@ -175,27 +175,6 @@ __device__ __forceinline__ uint32_t head_bits(const uint32_t *heads, uint32_t po
     return cnt >= 32 ? uint32_t(v) : uint32_t(v) & ((1u << cnt) - 1u);
 }
 
-// Warp-wide: the first index k in [lo, hi] with off[k] >= key, given that
-// off[lo-1] < key (or lo == 0) and that hi is a valid answer (off[hi] >= key,
-// or hi == N + 1).  Each round probes 32 evenly spaced indices below hi and
-// keeps the sub-interval between the last probe below the key and the first
-// one at or above it; probes stay inside [lo, hi), so inside offsets[0..N].
-__device__ __forceinline__ uint32_t warp_lower_bound(const uint32_t *off, uint32_t lo, uint32_t hi,
-                                                     uint32_t key, uint32_t lane) {
-    while (lo < hi) {
-        const uint32_t len = hi - lo;
-        const uint32_t step = (len + 31u) / 32u;
-        const uint64_t q = uint64_t(lo) + uint64_t(lane + 1u) * step - 1u;
-        const bool probe = q < hi;
-        const bool below = probe && __ldg(off + q) < key;
-        const uint32_t c = __reduce_add_sync(0xffffffffu, below ? 1u : 0u);
-        const uint32_t np = __reduce_add_sync(0xffffffffu, probe ? 1u : 0u);
-        if (c < np) hi = lo + (c + 1u) * step - 1u;  // probe c is at or above the key
-        lo = lo + c * step;                          // probes 0 .. c-1 are below it
-    }
-    return lo;
-}
-
 // Decoupled Fallback for the segmented scan: the descriptor tile p would
 // publish, from the values and the offsets.  The heads of a tile are the
 // offset values inside it; offsets are nondecreasing, so its last head is the

@@ -186,6 +186,33 @@ dwp_status dwp_scan_static_scratch(dwp_op op, dwp_mode mode, const void *d_in, v
                                    size_t n, dwp_stream stream);
 
 /*
+ * Segmented u32 addition reduction over CSR offsets ("GPUSegmentedScan"
+ * (luma.gl), section "Composition", which names the segmented reduction
+ * beside the segmented scan; the segments are those of "Contract"):
+ * d_out[s] = d_values[offsets[s]] + ... + d_values[offsets[s+1] - 1],
+ * wrapping modulo 2^32, and 0 for an empty segment.
+ *   d_values     n u32 (device, 16-byte aligned).
+ *   d_offsets    num_segments + 1 u32 (device, 4-byte aligned),
+ *                non-decreasing, d_offsets[num_segments] <= n.  Trusted, as
+ *                for dwp_segmented_scan_u32: other offsets give unspecified
+ *                sums, but every access stays inside the arrays.
+ *   d_out        num_segments u32 (device, 4-byte aligned), overlapping no
+ *                other argument.
+ *   d_scratch    NULL: *scratch_bytes receives the size needed (128 bytes:
+ *                a tile counter and the status word; this operation keeps
+ *                no per-tile state).  Otherwise at least that many bytes,
+ *                16-byte aligned, overlapping no other argument.
+ * The call clears d_out and the scratch on `stream` and launches one kernel;
+ * n == 0 or num_segments == 0 launches nothing.  Segment pieces that cross a
+ * tile edge are added with atomics: the result is exact (u32 addition wraps
+ * and commutes) and does not depend on the order.  Errors as for
+ * dwp_segmented_scan_u32.
+ */
+dwp_status dwp_segmented_reduce_u32(const uint32_t *d_values, const uint32_t *d_offsets,
+                                    size_t num_segments, uint32_t *d_out, size_t n,
+                                    void *d_scratch, size_t *scratch_bytes, dwp_stream stream);
+
+/*
  * First-order linear recurrence ("Parallel Prefix Sum (Scan), in depth",
  * section "What scan builds"): h[t] = a[t] * h[t-1] + b[t] with h[-1] = 0,
  * computed as a single-pass scan of the pairs (a[t], b[t]) under

@@ -152,3 +152,25 @@ def test_recurrence_size_query_and_validation(lib):
     assert R(a, b, h, n, ok, h + 16, need, 0)[0] == dwp.DWP_ERR_ALIASING   # scratch over h
     import ctypes
     assert lib.dwp_linear_recurrence_f32(None, None, None, 10, 1, None, None, None) == dwp.DWP_ERR_INVALID_VALUE
+
+
+def test_segreduce_size_query_and_validation(lib):
+    R = dwp.dwp_segmented_reduce_u32
+    for n in (0, 1, 1 << 20, (1 << 32) - 1):
+        st, b = R(0, 0, 0, 0, n, 0, 0, 0)
+        assert st == dwp.DWP_SUCCESS and b == 128  # no per-tile state
+    v, o, out, s = A, A + 8192, A + 16384, A + (1 << 30)
+    n, nseg = 1000, 10
+    assert R(v, o, nseg, out, 1 << 32, s, 128, 0)[0] == dwp.DWP_ERR_INVALID_VALUE
+    assert R(v, o, (1 << 32) - 1, out, n, s, 128, 0)[0] == dwp.DWP_ERR_INVALID_VALUE
+    assert R(v, o, nseg, out, n, s, 127, 0)[0] == dwp.DWP_ERR_SCRATCH_TOO_SMALL
+    assert R(0, o, nseg, out, n, s, 128, 0)[0] == dwp.DWP_ERR_INVALID_VALUE
+    assert R(v, 0, nseg, out, n, s, 128, 0)[0] == dwp.DWP_ERR_INVALID_VALUE
+    assert R(v, o, nseg, 0, n, s, 128, 0)[0] == dwp.DWP_ERR_INVALID_VALUE
+    assert R(v + 4, o, nseg, out, n, s, 128, 0)[0] == dwp.DWP_ERR_MISALIGNED
+    assert R(v, o + 2, nseg, out, n, s, 128, 0)[0] == dwp.DWP_ERR_MISALIGNED
+    assert R(v, o, nseg, out + 1, n, s, 128, 0)[0] == dwp.DWP_ERR_MISALIGNED
+    assert R(v, o, nseg, out, n, s + 4, 128, 0)[0] == dwp.DWP_ERR_MISALIGNED
+    assert R(v, o, nseg, v + 400, n, s, 128, 0)[0] == dwp.DWP_ERR_ALIASING    # out inside values
+    assert R(v, o, nseg, o + 8, n, s, 128, 0)[0] == dwp.DWP_ERR_ALIASING      # out over offsets
+    assert R(v, o, nseg, out, n, out + 16, 128, 0)[0] == dwp.DWP_ERR_ALIASING  # scratch over out
