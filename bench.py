@@ -407,6 +407,7 @@ def measure_secondary(dwp, lib, dev, stream, peaks, x, y, scratch, need) -> dict
     del xf
     out["u32_add_exclusive_2p20"] = measure_small(dwp, lib, dev, stream)
     out["fallback_one_silent_tile"] = measure_fallback(dwp, lib, stream, x, y, scratch, need)
+    out["lookback_window_ablation"] = measure_window_ablation(dwp, lib, stream, x, y, scratch, need)
     out["segscan_u32_exclusive"] = measure_segscan(dwp, lib, dev, stream, peaks)
     out["compact_16B_records"] = measure_compact(dwp, lib, dev, stream, peaks)
     out["linear_recurrence_f32"] = measure_recurrence(dwp, lib, dev, stream, peaks)
@@ -455,6 +456,35 @@ def measure_fallback(dwp, lib, stream, x, y, scratch, need, silent=5, polls=64, 
     return {"n": n, "silent_tile": silent, "fallback_polls": polls, "ms": ms,
             "healthy_ms": healthy, "added_us": (ms - healthy) * 1e3, "fallbacks_last_call": fb.value,
             "status": dwp.dwp_status_string(status)}
+
+
+def measure_window_ablation(dwp, lib, stream, x, y, scratch, need, steps=50,
+                            windows=(0, 32, 128, 1024)) -> dict:
+    """Bounded look-back window against the unbounded one on the headline call:
+    healthy, and with tile 5 silent until a successor rescues it after 64
+    polls (every later tile then folds a long chain of aggregates: the case a
+    window bounds)."""
+    import ctypes
+    n = x.numel()
+    sb = ctypes.c_size_t(need)
+    st_ptr = ctypes.c_void_p(int(stream.cuda_stream))
+    args = (dwp.DWP_U32_ADD, ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(y.data_ptr()), n,
+            ctypes.c_void_p(scratch.data_ptr()), ctypes.byref(sb), st_ptr)
+    res = {"n": n, "note": "window 0 = unbounded (the default); ms per call"}
+    try:
+        for w in windows:
+            lib.dwp_set_lookback_window(w)
+            healthy = time_calls(lambda: lib.dwp_scan_exclusive(*args), steps, 3, stream)
+            lib.dwp_debug_set_fault(5, 0, 64)
+            stalled = time_calls(lambda: lib.dwp_scan_exclusive(*args), steps, 3, stream)
+            lib.dwp_debug_set_fault(0xFFFFFFFF, 0, 0)
+            status = lib.dwp_read_status(ctypes.c_void_p(scratch.data_ptr()), st_ptr)
+            res["window_%d" % w] = {"healthy_ms": healthy, "one_silent_tile_ms": stalled,
+                                    "status": dwp.dwp_status_string(status)}
+    finally:
+        lib.dwp_set_lookback_window(0)
+        lib.dwp_debug_set_fault(0xFFFFFFFF, 0, 0)
+    return res
 
 
 def run_only(args) -> None:

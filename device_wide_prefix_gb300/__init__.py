@@ -51,6 +51,7 @@ EXPORTS = [
     "dwp_status_string",
     "dwp_version",
     "dwp_debug_set_fault",
+    "dwp_set_lookback_window",
     "dwp_scan_static_scratch",
 ]
 
@@ -97,6 +98,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dwp_version.restype = c.c_int
     lib.dwp_debug_set_fault.argtypes = [c.c_uint32, c.c_uint32, c.c_uint32]
     lib.dwp_debug_set_fault.restype = c.c_int
+    lib.dwp_set_lookback_window.argtypes = [c.c_uint32]
+    lib.dwp_set_lookback_window.restype = c.c_int
     lib.dwp_scan_static_scratch.argtypes = [c.c_int, c.c_int, P, P, S, P]
     lib.dwp_scan_static_scratch.restype = c.c_int
     if path == LIB_PATH:
@@ -191,6 +194,11 @@ def dwp_version() -> int:
 def dwp_debug_set_fault(never_publish_tile: int, spin_limit: int, fallback_polls: int = 0) -> int:
     return load().dwp_debug_set_fault(never_publish_tile & 0xFFFFFFFF, spin_limit,
                                       fallback_polls & 0xFFFFFFFF)
+
+
+def dwp_set_lookback_window(tiles: int) -> int:
+    """dwp.h dwp_set_lookback_window: 0 unbounded (default), else the window in tiles."""
+    return load().dwp_set_lookback_window(int(tiles) & 0xFFFFFFFF)
 
 
 def status_string(status: int) -> str:

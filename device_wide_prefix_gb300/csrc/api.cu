@@ -286,6 +286,11 @@ const char *dwp_status_string(dwp_status status) {
 
 int dwp_version(void) { return 100; }
 
+dwp_status dwp_set_lookback_window(uint32_t tiles) {
+    set_lookback_window(tiles);
+    return DWP_SUCCESS;
+}
+
 dwp_status dwp_read_fallbacks(const void *d_scratch, dwp_stream stream, uint32_t *count) {
     if (!d_scratch || !count) return DWP_ERR_INVALID_VALUE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

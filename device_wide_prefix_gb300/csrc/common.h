@@ -31,14 +31,17 @@ constexpr uint32_t kPipeWaitLimit = 1u << 24;     // mbarrier polls (>1 s with b
 // far above any wait of a healthy run).
 constexpr uint32_t kDefaultFallbackPolls = 1u << 12;
 
-// Test hooks carried into every launch (see dwp_debug_set_fault).
-struct FaultConfig {
+// Settings carried into every launch: the test hooks of dwp_debug_set_fault
+// and the look-back window of dwp_set_lookback_window.
+struct LaunchKnobs {
     uint32_t never_publish_tile;  // UINT32_MAX: none
     uint32_t spin_limit;          // look-back polls before giving up
     uint32_t fallback_polls;      // polls before a Decoupled Fallback; 0: never
+    uint32_t lookback_window;     // tiles folded between intermediate publications; 0: unbounded
 };
 
-FaultConfig current_fault_config();
+LaunchKnobs current_launch_knobs();
 void set_fault_config(uint32_t never_publish_tile, uint32_t spin_limit, uint32_t fallback_polls);
+void set_lookback_window(uint32_t tiles);
 
 }  // namespace dwp

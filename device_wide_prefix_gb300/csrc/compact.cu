@@ -163,7 +163,7 @@ template <class C>
 __global__ void __launch_bounds__(C::kThreads, 1)
     compact_kernel(const uint4 *recs, const uint8_t *flags, uint64_t n, uint4 *out,
                    uint32_t *count, uint32_t num_tiles, ScratchHeader *hdr, uint64_t *desc,
-                   FaultConfig fault) {
+                   LaunchKnobs fault) {
     using Op = OpU32Add;
     constexpr int NW = C::kWarps, IT = C::kItems, TILE = C::kTile;
     constexpr int SOUT = C::kOut, RING = C::kRing, TW = C::kTileWarps;
@@ -307,7 +307,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             if (t != 0)
                 rc = lookback<Op, C::kLookK>(desc, t, lane, fault.spin_limit, fault.fallback_polls,
                                              CompactRescue<TILE>{flags, n}, &hdr->fallbacks,
-                                             sm.lb_scratch(i), &carry);
+                                             fault.lookback_window, total,
+                                             t != fault.never_publish_tile, sm.lb_scratch(i), &carry);
             if (lane == 0) {
                 if (rc == 0) {
                     if (t != 0 && t != fault.never_publish_tile)
@@ -434,7 +435,7 @@ uint32_t compact_tile_records() { return CmpCfg::kTile; }
 cudaError_t launch_compact(const void *records, const uint8_t *flags, uint64_t n, void *out,
                            uint32_t *count, void *scratch, cudaStream_t stream) {
     using C = CmpCfg;
-    const FaultConfig fault = current_fault_config();
+    const LaunchKnobs fault = current_launch_knobs();
     auto kern = compact_kernel<C>;
     const int dev_blocks = device_blocks(reinterpret_cast<const void *>(kern), C::kThreads,
                                          C::kSmemBytes);

@@ -230,6 +230,9 @@ __device__ __forceinline__ void record_error(ScratchHeader *hdr, uint32_t code) 
 // abandoned after a timeout; readers treat it as terminal and propagate it.
 
 enum : uint32_t { kInvalid = 0u, kAggregate = 1u, kPrefix = 2u, kPoison = 3u };
+// State kSpan0 + d (d >= 2): an intermediate published by a bounded-window
+// look-back; its value combines the d tiles ending at this one.
+constexpr uint32_t kSpan0 = 4u;
 
 __device__ __forceinline__ uint64_t make_desc(uint32_t state, uint32_t bits) {
     return (static_cast<uint64_t>(state) << 32) | bits;
@@ -325,6 +328,17 @@ __device__ __forceinline__ uint32_t warp_lower_bound(const uint32_t *off, uint32
 // input must stay unmodified for the whole launch: callers disable the
 // fallback (fallback_polls = 0) for an in-place scan.
 //
+// Bounded window ("Single-Pass Prefix Scan with Decoupled Look-Back",
+// section "Why the work stays linear"): with window > 0 and `publish`, each
+// time the look-back of tile t has folded `window` more tiles without
+// reaching a prefix, lane 0 publishes an intermediate descriptor for t: the
+// combination of everything folded so far with t's own aggregate `own`, and
+// the number d of tiles it covers (t - d + 1 .. t), as state kSpan0 + d.  A
+// look-back that meets an intermediate as the nearest stop of its window
+// folds it and jumps d tiles back at once.  Folds happen a window of K*32
+// tiles at a time, so the effective window is a multiple of K*32.  A tile
+// that has already published its prefix must pass publish = false.
+//
 // Returns 0 and the exclusive prefix of tile t in *carry_out; 1 if the
 // nearest terminal descriptor is poison; 2 if the poll limit ran out.
 
@@ -332,13 +346,15 @@ template <class Op, int K, class Rescue>
 __device__ __forceinline__ int lookback(uint64_t *desc, uint32_t t, uint32_t lane,
                                         uint32_t spin_limit, uint32_t fallback_polls,
                                         const Rescue &rescue, uint32_t *fallbacks,
+                                        uint32_t window, uint32_t own, bool publish,
                                         uint32_t *scratch, typename Op::T *carry_out) {
     using T = typename Op::T;
     static_assert(Op::kCommutative, "the look-back combines per lane first");
-    static_assert(K * 32 < (1 << 30), "window positions must fit the key");
+    static_assert(K * 32 < (1 << 29), "window positions must fit the key");
     T carry = Op::identity();
     int64_t base = static_cast<int64_t>(t) - 1;
     uint32_t polls = 0;
+    uint64_t next_pub = window;  // folded tiles at which the next intermediate goes out
     while (true) {
         uint64_t d[K];
 #pragma unroll
@@ -349,20 +365,23 @@ __device__ __forceinline__ int lookback(uint64_t *desc, uint32_t t, uint32_t lan
         }
         uint32_t tkey, imin, stalled = 0;
         while (true) {
-            // key of the nearest terminal descriptor = 2*position + poison bit
+            // key of the nearest stop = 4*position + kind (0 prefix, 1
+            // poison, 2 intermediate)
             uint32_t my_t = 0xffffffffu, my_i = 0xffffffffu;
 #pragma unroll
             for (int i = K - 1; i >= 0; --i) {
                 const uint32_t st = desc_state(d[i]);
                 const uint32_t p = 32u * i + lane;
-                if (st == kPrefix || st == kPoison) my_t = (p << 1) | (st == kPoison ? 1u : 0u);
+                if (st == kPrefix) my_t = p << 2;
+                else if (st == kPoison) my_t = (p << 2) | 1u;
+                else if (st >= kSpan0) my_t = (p << 2) | 2u;
                 if (st == kInvalid) my_i = p;
             }
             tkey = __reduce_min_sync(0xffffffffu, my_t);
             imin = __reduce_min_sync(0xffffffffu, my_i);
-            if (tkey != 0xffffffffu ? imin > (tkey >> 1) : imin == 0xffffffffu) break;
+            if (tkey != 0xffffffffu ? imin > (tkey >> 2) : imin == 0xffffffffu) break;
             if (++polls >= spin_limit) return 2;
-            const uint32_t lim = tkey != 0xffffffffu ? (tkey >> 1) : 32u * K;
+            const uint32_t lim = tkey != 0xffffffffu ? (tkey >> 2) : 32u * K;
             if (fallback_polls != 0u && ++stalled >= fallback_polls) {
                 stalled = 0;
 #pragma unroll
@@ -397,15 +416,27 @@ __device__ __forceinline__ int lookback(uint64_t *desc, uint32_t t, uint32_t lan
                     d[i] = ld_relaxed_gpu(desc + idx);
             }
         }
-        if (tkey != 0xffffffffu && (tkey & 1u)) return 1;
-        const uint32_t last = tkey != 0xffffffffu ? (tkey >> 1) : 0xffffffffu;
+        const uint32_t kind = tkey != 0xffffffffu ? (tkey & 3u) : 3u;
+        if (kind == 1u) return 1;
+        const uint32_t last = tkey != 0xffffffffu ? (tkey >> 2) : 0xffffffffu;
         T acc = Op::identity();
+        uint32_t span = 0;
 #pragma unroll
-        for (int i = 0; i < K; ++i)
+        for (int i = 0; i < K; ++i) {
             if (32u * i + lane <= last) acc = Op::combine(acc, Op::from_bits(desc_bits(d[i])));
+            if (32u * i + lane == last && kind == 2u) span = desc_state(d[i]) - kSpan0;
+        }
         carry = Op::combine(Op::warp_reduce(acc, lane, scratch), carry);
-        if (tkey != 0xffffffffu) break;
-        base -= 32 * K;
+        if (kind == 0u) break;
+        // the intermediate at position `last` covers `span` tiles ending at it
+        base -= kind == 2u ? int64_t(last) + int64_t(__reduce_max_sync(0xffffffffu, span)) : 32 * K;
+        const uint64_t folded = uint64_t(int64_t(t) - 1 - base);
+        if (window != 0u && publish && folded >= next_pub) {
+            if (lane == 0)
+                st_relaxed_gpu(desc + t, make_desc(kSpan0 + uint32_t(folded) + 1u,
+                                                   Op::to_bits(Op::combine(carry, Op::from_bits(own)))));
+            next_pub = folded + window;
+        }
     }
     *carry_out = carry;
     return 0;

@@ -16,6 +16,7 @@ std::map<std::pair<int, const void *>, int> g_blocks;
 std::atomic<uint32_t> g_never_publish{0xffffffffu};
 std::atomic<uint32_t> g_spin_limit{0u};
 std::atomic<uint32_t> g_fallback_polls{0u};
+std::atomic<uint32_t> g_lookback_window{0u};
 }  // namespace
 
 int device_blocks(const void *kernel, int threads, size_t smem_bytes) {
@@ -39,15 +40,18 @@ int device_blocks(const void *kernel, int threads, size_t smem_bytes) {
     return blocks;
 }
 
-FaultConfig current_fault_config() {
-    FaultConfig f;
+LaunchKnobs current_launch_knobs() {
+    LaunchKnobs f;
     f.never_publish_tile = g_never_publish.load();
     const uint32_t lim = g_spin_limit.load();
     f.spin_limit = lim ? lim : kDefaultSpinLimit;
     const uint32_t fb = g_fallback_polls.load();
     f.fallback_polls = fb == 0u ? kDefaultFallbackPolls : (fb == 0xffffffffu ? 0u : fb);
+    f.lookback_window = g_lookback_window.load();
     return f;
 }
+
+void set_lookback_window(uint32_t tiles) { g_lookback_window.store(tiles); }
 
 void set_fault_config(uint32_t never_publish_tile, uint32_t spin_limit, uint32_t fallback_polls) {
     g_never_publish.store(never_publish_tile);

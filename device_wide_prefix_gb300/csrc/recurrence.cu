@@ -323,7 +323,7 @@ __device__ __forceinline__ int lookback_affine(uint64_t *desc, uint32_t t, uint3
 template <bool INCL, class C>
 __global__ void __launch_bounds__(C::kThreads, 1)
     recurrence_kernel(const float *ga, const float *gb, float *out, uint64_t n, uint32_t num_tiles,
-                      ScratchHeader *hdr, uint64_t *desc, FaultConfig fault) {
+                      ScratchHeader *hdr, uint64_t *desc, LaunchKnobs fault) {
     constexpr int NW = C::kWarps, ITEMS = C::kItems, TILE = C::kTile;
     constexpr int SIN = C::kIn, SOUT = C::kOut, RING = C::kRing, LW = C::kLookers;
     constexpr int WE = C::kWarpElems, AHEAD = C::kAhead;
@@ -727,7 +727,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 
 template <bool INCL>
 cudaError_t launch_rec(const float *a, const float *b, float *h, uint64_t n, void *scratch,
-                       cudaStream_t stream, const FaultConfig &fault) {
+                       cudaStream_t stream, const LaunchKnobs &fault) {
     using C = RecCfg;
     auto kern = recurrence_kernel<INCL, C>;
     const int dev_blocks = device_blocks(reinterpret_cast<const void *>(kern), C::kThreads,
@@ -747,7 +747,7 @@ uint32_t recurrence_tile_elems() { return RecCfg::kTile; }
 
 cudaError_t launch_recurrence(const float *a, const float *b, float *h, uint64_t n, bool inclusive,
                               void *scratch, cudaStream_t stream) {
-    FaultConfig fault = current_fault_config();
+    LaunchKnobs fault = current_launch_knobs();
     // in place, the inputs of a stalled tile may already be output: no fallback
     if (h == a || h == b) fault.fallback_polls = 0u;
     return inclusive ? launch_rec<true>(a, b, h, n, scratch, stream, fault)

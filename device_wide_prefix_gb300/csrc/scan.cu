@@ -204,7 +204,7 @@ struct ScanRescue {
 template <class Op, bool INCL, class C>
 __global__ void __launch_bounds__(C::kThreads, 1)
     scan_kernel(const typename Op::T *in, typename Op::T *out, uint64_t n, uint32_t num_tiles,
-                ScratchHeader *hdr, uint64_t *desc, FaultConfig fault) {
+                ScratchHeader *hdr, uint64_t *desc, LaunchKnobs fault) {
     using T = typename Op::T;
     constexpr int NW = C::kWarps, ITEMS = C::kItems, TILE = C::kTile;
     constexpr int SIN = C::kIn, SOUT = C::kOut, RING = C::kRing, LW = C::kLookers;
@@ -439,7 +439,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             if (rc == 0 && t != 0)
                 rc = lookback<Op, C::kLookK>(desc, t, lane, fault.spin_limit, fault.fallback_polls,
                                              ScanRescue<Op, TILE>{in, n}, &hdr->fallbacks,
-                                             sm.lb_scratch(int(j)), &carry);
+                                             fault.lookback_window, *sm.agg(i),
+                                             t != fault.never_publish_tile, sm.lb_scratch(int(j)),
+                                             &carry);
             if (lane == 0) {
                 if (rc == 0) {
                     if (t != 0 && t != fault.never_publish_tile)
@@ -600,7 +602,7 @@ namespace {
 
 template <class Op, bool INCL>
 cudaError_t launch_one(const void *in, void *out, uint64_t n, void *scratch, cudaStream_t stream,
-                       const FaultConfig &fault) {
+                       const LaunchKnobs &fault) {
     using C = ScanCfg;
     auto kern = scan_kernel<Op, INCL, C>;
     const int dev_blocks = device_blocks(reinterpret_cast<const void *>(kern), C::kThreads,
@@ -622,7 +624,7 @@ uint32_t scan_tile_elems() { return ScanCfg::kTile; }
 
 cudaError_t launch_scan(dwp_op op, bool inclusive, const void *in, void *out, uint64_t n,
                         void *scratch, cudaStream_t stream) {
-    FaultConfig fault = current_fault_config();
+    LaunchKnobs fault = current_launch_knobs();
     // in place, the input of a stalled tile may already be output: no fallback
     if (in == out) fault.fallback_polls = 0u;
     switch (op) {

@@ -212,7 +212,7 @@ template <bool INCL, class C>
 __global__ void __launch_bounds__(C::kThreads, 1)
     segscan_kernel(const uint32_t *in, const uint32_t *off, uint32_t nseg, uint32_t *out,
                    uint64_t n, uint32_t num_tiles, ScratchHeader *hdr, uint64_t *desc,
-                   FaultConfig fault) {
+                   LaunchKnobs fault) {
     using Op = OpU32Add;
     constexpr int NW = C::kWarps, ITEMS = C::kItems, TILE = C::kTile;
     constexpr int SIN = C::kIn, SOUT = C::kOut, RING = C::kRing, LW = C::kLookers;
@@ -527,7 +527,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             if (rc == 0 && t != 0 && ld_volatile_smem(sm.first_head(i)) == 0u)
                 rc = lookback<Op, C::kLookK>(desc, t, lane, fault.spin_limit, fault.fallback_polls,
                                              SegRescue{in, off, nseg, n, uint32_t(TILE)},
-                                             &hdr->fallbacks, sm.lb_scratch(i), &carry);
+                                             &hdr->fallbacks, fault.lookback_window, *sm.agg(i),
+                                             !ah && t != fault.never_publish_tile, sm.lb_scratch(i),
+                                             &carry);
             if (lane == 0) {
                 if (rc == 0) {
                     if (t != 0 && !ah && t != fault.never_publish_tile)
@@ -691,7 +693,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 template <bool INCL>
 cudaError_t launch_seg(const uint32_t *values, const uint32_t *offsets, uint32_t nseg,
                        uint32_t *out, uint64_t n, void *scratch, cudaStream_t stream,
-                       const FaultConfig &fault) {
+                       const LaunchKnobs &fault) {
     using C = SegCfg;
     auto kern = segscan_kernel<INCL, C>;
     const int dev_blocks = device_blocks(reinterpret_cast<const void *>(kern), C::kThreads,
@@ -713,7 +715,7 @@ uint32_t segscan_tile_elems() { return SegCfg::kTile; }
 cudaError_t launch_segscan(const uint32_t *values, const uint32_t *offsets, uint32_t nseg,
                            uint32_t *out, uint64_t n, bool inclusive, void *scratch,
                            cudaStream_t stream) {
-    const FaultConfig fault = current_fault_config();
+    const LaunchKnobs fault = current_launch_knobs();
     return inclusive ? launch_seg<true>(values, offsets, nseg, out, n, scratch, stream, fault)
                      : launch_seg<false>(values, offsets, nseg, out, n, scratch, stream, fault);
 }

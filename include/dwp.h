@@ -262,6 +262,22 @@ const char *dwp_status_string(dwp_status status);
 int dwp_version(void);
 
 /*
+ * Look-back window, a tuning setting for every later call in this process
+ * ("Single-Pass Prefix Scan with Decoupled Look-Back", section "Why the work
+ * stays linear"): 0 (the default) lets a look-back follow the chain of
+ * predecessors as far as it goes.  tiles > 0 bounds it: each time a tile's
+ * look-back has folded `tiles` more predecessors without reaching a prefix,
+ * it publishes an intermediate descriptor (the sum so far with its own
+ * aggregate, and how many tiles that covers), and a later look-back that
+ * meets it jumps over that many tiles at once.  Folds go 32 tiles at a
+ * time, so the window is effectively rounded up to a multiple of 32.
+ * Applies to the plain and segmented scans and to compaction; results do not
+ * depend on it (bit for bit for the integer operations).  Not thread-safe;
+ * affects every device.  Always DWP_SUCCESS.
+ */
+dwp_status dwp_set_lookback_window(uint32_t tiles);
+
+/*
  * Test hook, not for production use.  For every later call in this process
  * until reset:
  *   - the tile with index `never_publish_tile` does its work but never

@@ -148,3 +148,17 @@ def test_fallback_rescues_a_silent_tile(ref, silent):
     got = out.cpu().numpy().view(np.uint32)
     assert int(cnt.item()) == k
     assert (got[:k] == want[:k]).all() and (got[k:] == SENTINEL).all()
+
+
+def test_bounded_window_same_result(ref):
+    n = 1500 * tile() + 5
+    rec = synth.records(n, seed=903)
+    flags = synth.keep_flags(n, 0.3, seed=904)
+    try:
+        dwp.dwp_set_lookback_window(64)
+        for silent in (0xFFFFFFFF, 600):
+            dwp.dwp_debug_set_fault(silent, 0, 64)
+            check(ref, rec, flags)
+    finally:
+        dwp.dwp_set_lookback_window(0)
+        dwp.dwp_debug_set_fault(0xFFFFFFFF, 0, 0)

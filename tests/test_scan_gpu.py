@@ -244,3 +244,28 @@ def test_no_fallback_in_a_healthy_run(ref):
         dwp.scan_exclusive(x, "u32_add", scratch=scratch)
         assert dwp.read_status(scratch) == dwp.DWP_SUCCESS
         assert dwp.read_fallbacks(scratch) == 0
+
+
+# ------------------------------------------------ bounded look-back window
+
+@pytest.mark.parametrize("window", [1, 32, 100])
+@pytest.mark.parametrize("op,inclusive", [("u32_add", False), ("u32_max", True), ("f32_add", True)])
+def test_bounded_window_same_result(ref, window, op, inclusive):
+    """A bounded look-back window publishes intermediates and jumps over them;
+    the output is the oracle's either way.  A silent tile rescued after 64
+    polls makes every tile behind it fold a long chain of aggregates, so the
+    intermediates are really published and followed."""
+    n = 3000 * tile() + 77
+    x = synth.f32_values(n, 31) if op == "f32_add" else synth.u32_full_values(n, 31)
+    t = torch.from_numpy(x.view(np.float32 if op == "f32_add" else np.int32)).cuda()
+    scratch = dwp.alloc_scratch(dwp.scan_scratch_bytes(n, op), t.device)
+    try:
+        dwp.dwp_set_lookback_window(window)
+        for silent in (0xFFFFFFFF, 1234):
+            dwp.dwp_debug_set_fault(silent, 0, 64)
+            y = (dwp.scan_inclusive if inclusive else dwp.scan_exclusive)(t, op, scratch=scratch)
+            assert dwp.read_status(scratch) == dwp.DWP_SUCCESS
+            check(ref, x, op, inclusive, y.cpu().numpy().view(x.dtype))
+    finally:
+        dwp.dwp_set_lookback_window(0)
+        dwp.dwp_debug_set_fault(0xFFFFFFFF, 0, 0)

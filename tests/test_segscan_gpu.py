@@ -174,3 +174,24 @@ def test_fallback_rescues_silent_tiles(ref):
         # a head (then no tile needs the silent tile's descriptor)
         if not np.isin(starts[silent + 1], offsets):
             assert fb >= 1
+
+
+def test_bounded_window_same_result(ref):
+    """Bounded look-back window on the segmented scan (tiles that hold a head
+    never publish an intermediate over their prefix); bit-exact, with and
+    without a silent tile."""
+    T = tile()
+    n = 1500 * T + 19
+    values = synth.u32_byte_values(n, seed=43)
+    offsets = synth.segment_offsets(n, seed=44)
+    want = ref.segmented_scan_u32(values, offsets, True, out=np.full(n, SENTINEL, np.uint32))
+    try:
+        dwp.dwp_set_lookback_window(32)
+        for silent in (0xFFFFFFFF, 700):
+            dwp.dwp_debug_set_fault(silent, 0, 64)
+            got = gpu_seg(values, offsets, True)
+            bad = np.nonzero(got != want)[0]
+            assert bad.size == 0, "silent %d: mismatch at %s" % (silent, bad[:5])
+    finally:
+        dwp.dwp_set_lookback_window(0)
+        dwp.dwp_debug_set_fault(0xFFFFFFFF, 0, 0)
