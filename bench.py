@@ -406,6 +406,7 @@ def measure_secondary(dwp, lib, dev, stream, peaks, x, y, scratch, need) -> dict
                      "frac": gbs / peaks["hbm_gbs"]}
     del xf
     out["u32_add_exclusive_2p20"] = measure_small(dwp, lib, dev, stream)
+    out["single_pass_vs_two_level"] = measure_two_level(dwp, lib, dev, stream)
     out["fallback_one_silent_tile"] = measure_fallback(dwp, lib, stream, x, y, scratch, need)
     out["lookback_window_ablation"] = measure_window_ablation(dwp, lib, stream, x, y, scratch, need)
     out["segscan_u32_exclusive"] = measure_segscan(dwp, lib, dev, stream, peaks)
@@ -433,6 +434,33 @@ def measure_small(dwp, lib, dev, stream, log2n=20, steps=2000, warmup=20) -> dic
     return {"n": n, "us": ms * 1e3, "Gelem_s": n / (ms * 1e-3) / 1e9,
             "workload": "u32 exclusive sum scan, n=2^%d values in [0,16) (SplitMix64 seed 0xD3B00001), "
                         "L2-resident: launch-bound, not an HBM figure" % log2n}
+
+
+def measure_two_level(dwp, lib, dev, stream, log2ns=(12, 14, 16, 18, 20, 22, 24, 26), steps=500) -> dict:
+    """u32 exclusive add by the single-pass look-back scan and by the
+    two-level three-launch form, microseconds per call, back to back."""
+    import ctypes
+    import torch
+    st_ptr = ctypes.c_void_p(int(stream.cuda_stream))
+    res = {"unit": "us per call"}
+    for lg in log2ns:
+        n = 1 << lg
+        x = torch.from_numpy(synth.u32_small_values(n).view(np.int32)).to(dev)
+        y = torch.empty_like(x)
+        row = {}
+        for name, fn in (("single_pass", lib.dwp_scan_exclusive), ("two_level", lib.dwp_scan_two_level)):
+            sb = ctypes.c_size_t(0)
+            if name == "single_pass":
+                fn(0, None, None, n, None, ctypes.byref(sb), None)
+            else:
+                fn(0, 0, None, None, n, None, ctypes.byref(sb), None)
+            scratch = torch.empty(sb.value, dtype=torch.uint8, device=dev)
+            common = (ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(y.data_ptr()), n,
+                      ctypes.c_void_p(scratch.data_ptr()), ctypes.byref(sb), st_ptr)
+            args = (0,) + common if name == "single_pass" else (0, 0) + common
+            row[name] = time_calls(lambda: fn(*args), max(20, steps >> max(0, lg - 20)), 5, stream) * 1e3
+        res["2^%d" % lg] = row
+    return res
 
 
 def measure_fallback(dwp, lib, stream, x, y, scratch, need, silent=5, polls=64, steps=20) -> dict:

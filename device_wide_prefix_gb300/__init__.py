@@ -53,6 +53,7 @@ EXPORTS = [
     "dwp_debug_set_fault",
     "dwp_set_lookback_window",
     "dwp_scan_static_scratch",
+    "dwp_scan_two_level",
 ]
 
 _lib = None
@@ -102,6 +103,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dwp_set_lookback_window.restype = c.c_int
     lib.dwp_scan_static_scratch.argtypes = [c.c_int, c.c_int, P, P, S, P]
     lib.dwp_scan_static_scratch.restype = c.c_int
+    lib.dwp_scan_two_level.argtypes = [c.c_int, c.c_int, P, P, S, P, Z, P]
+    lib.dwp_scan_two_level.restype = c.c_int
     if path == LIB_PATH:
         _lib = lib
     return lib
@@ -126,6 +129,14 @@ def dwp_scan_exclusive(op, d_in, d_out, n, d_scratch, scratch_bytes, stream):
 def dwp_scan_inclusive(op, d_in, d_out, n, d_scratch, scratch_bytes, stream):
     """dwp.h dwp_scan_inclusive; returns (status, scratch_bytes after the call)."""
     return _scan_entry("dwp_scan_inclusive", op, d_in, d_out, n, d_scratch, scratch_bytes, stream)
+
+
+def dwp_scan_two_level(op, mode, d_in, d_out, n, d_scratch, scratch_bytes, stream):
+    """dwp.h dwp_scan_two_level; returns (status, scratch_bytes after the call)."""
+    sb = ctypes.c_size_t(scratch_bytes)
+    st = load().dwp_scan_two_level(int(op), int(mode), d_in or None, d_out or None, n,
+                                   d_scratch or None, ctypes.byref(sb), stream or None)
+    return st, sb.value
 
 
 def dwp_segmented_scan_u32(d_values, d_offsets, num_segments, d_out, n, mode, d_scratch,
@@ -274,6 +285,33 @@ def scan_exclusive(x, op: str = "u32_add", out=None, scratch=None, stream=None):
 def scan_inclusive(x, op: str = "u32_add", out=None, scratch=None, stream=None):
     """Inclusive scan of a contiguous CUDA tensor (int32/uint32 bits or float32)."""
     return _scan(True, x, op, out, scratch, stream)
+
+
+def two_level_scratch_bytes(n: int) -> int:
+    st, b = dwp_scan_two_level(DWP_U32_ADD, DWP_EXCLUSIVE, None, None, n, None, 0, None)
+    _check(st, "two-level scan scratch size query")
+    return b
+
+
+def scan_two_level(x, op: str = "u32_add", inclusive: bool = False, out=None, scratch=None,
+                   stream=None):
+    """The plain scan by the two-level, three-launch form (n <= 2^26)."""
+    torch = _torch()
+    if op not in OPS:
+        raise ValueError("unknown op %r" % op)
+    if not x.is_cuda or not x.is_contiguous() or x.element_size() != 4:
+        raise ValueError("x must be a contiguous CUDA tensor of 4-byte elements")
+    n = x.numel()
+    if out is None:
+        out = torch.empty_like(x)
+    if scratch is None:
+        scratch = alloc_scratch(two_level_scratch_bytes(n), x.device)
+    with torch.cuda.device(x.device):
+        st, _ = dwp_scan_two_level(OPS[op], DWP_INCLUSIVE if inclusive else DWP_EXCLUSIVE,
+                                   x.data_ptr(), out.data_ptr(), n, scratch.data_ptr(),
+                                   scratch.numel(), _stream_of(x, stream))
+    _check(st, "dwp_scan_two_level")
+    return out
 
 
 def segmented_scan_scratch_bytes(n: int) -> int:

@@ -58,6 +58,41 @@ dwp_status scan_common(bool inclusive, dwp_op op, const void *in, void *out, siz
     return DWP_SUCCESS;
 }
 
+dwp_status two_level_common(dwp_op op, dwp_mode mode, const void *in, void *out, size_t n,
+                            void *scratch, size_t *scratch_bytes, dwp_stream stream) {
+    if (!scratch_bytes) return DWP_ERR_INVALID_VALUE;
+    const int iop = static_cast<int>(op), m = static_cast<int>(mode);
+    if (iop != DWP_U32_ADD && iop != DWP_F32_ADD && iop != DWP_U32_MAX) return DWP_ERR_INVALID_VALUE;
+    if (m != DWP_EXCLUSIVE && m != DWP_INCLUSIVE) return DWP_ERR_INVALID_VALUE;
+    if (uint64_t(n) > two_level_max_n()) return DWP_ERR_INVALID_VALUE;
+    const uint64_t blocks = ceil_div(n, two_level_chunk());
+    const size_t need = kHeaderBytes + size_t(4u * blocks);  // one u32 total per block
+    if (!scratch) {
+        *scratch_bytes = need;
+        return DWP_SUCCESS;
+    }
+    if (*scratch_bytes < need) return DWP_ERR_SCRATCH_TOO_SMALL;
+    if (n > 0 && (!in || !out)) return DWP_ERR_INVALID_VALUE;
+    if (!aligned16(scratch) || (n > 0 && (!aligned16(in) || !aligned16(out))))
+        return DWP_ERR_MISALIGNED;
+    const uint64_t bytes = uint64_t(n) * 4u;
+    if (in != out && overlap(in, bytes, out, bytes)) return DWP_ERR_ALIASING;
+    if (overlap(scratch, need, in, bytes) || overlap(scratch, need, out, bytes))
+        return DWP_ERR_ALIASING;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // only the status word needs clearing: the totals are written before use
+    if (cudaMemsetAsync(scratch, 0, kHeaderBytes, s) != cudaSuccess) {
+        cudaGetLastError();
+        return DWP_ERR_CUDA;
+    }
+    if (n == 0) return DWP_SUCCESS;
+    if (launch_two_level(op, m == DWP_INCLUSIVE, in, out, n, scratch, s) != cudaSuccess) {
+        cudaGetLastError();
+        return DWP_ERR_CUDA;
+    }
+    return DWP_SUCCESS;
+}
+
 bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 dwp_status segscan_common(const uint32_t *values, const uint32_t *offsets, size_t nseg,
@@ -254,6 +289,11 @@ dwp_status dwp_linear_recurrence_f32(const float *d_a, const float *d_b, float *
                                      dwp_mode mode, void *d_scratch, size_t *scratch_bytes,
                                      dwp_stream stream) {
     return recurrence_common(d_a, d_b, d_h, n, mode, d_scratch, scratch_bytes, stream);
+}
+
+dwp_status dwp_scan_two_level(dwp_op op, dwp_mode mode, const void *d_in, void *d_out, size_t n,
+                              void *d_scratch, size_t *scratch_bytes, dwp_stream stream) {
+    return two_level_common(op, mode, d_in, d_out, n, d_scratch, scratch_bytes, stream);
 }
 
 dwp_status dwp_read_status(const void *d_scratch, dwp_stream stream) {

@@ -32,6 +32,14 @@ uint32_t compact_tile_records();
 cudaError_t launch_compact(const void *records, const uint8_t *flags, uint64_t n, void *out,
                            uint32_t *count, void *scratch, cudaStream_t stream);
 
+// Largest n and elements per block of the two-level (three-launch) scan.
+uint64_t two_level_max_n();
+uint32_t two_level_chunk();
+// The three launches of the two-level scan; the scratch holds the 128-byte
+// header and then one u32 total per block.
+cudaError_t launch_two_level(dwp_op op, bool inclusive, const void *in, void *out, uint64_t n,
+                             void *scratch, cudaStream_t stream);
+
 // Rows per tile of the segmented reduction kernel.
 uint32_t segreduce_tile_elems();
 // One launch of the segmented u32 reduction (out already cleared, scratch

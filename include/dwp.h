@@ -186,6 +186,23 @@ dwp_status dwp_scan_static_scratch(dwp_op op, dwp_mode mode, const void *d_in, v
                                    size_t n, dwp_stream stream);
 
 /*
+ * The same scans as dwp_scan_exclusive / dwp_scan_inclusive (`mode` picks
+ * one) by the two-level form in three launches: block totals, a one-block
+ * scan of the totals, then each block scans its chunk again from its total
+ * ("Single-Pass Prefix Scan with Decoupled Look-Back", sections "The
+ * two-level decomposition" and "When not to use it").  No descriptors and
+ * no spinning; the input is read twice.  For small inputs and for
+ * comparison with the single-pass scan.
+ *   n            at most 2^26 (DWP_ERR_INVALID_VALUE above).
+ *   d_scratch    NULL: *scratch_bytes receives the size needed (128 bytes
+ *                plus 4 bytes per 4096-element block).  Never more than
+ *                dwp_scan_exclusive asks for the same n.
+ * Pointers, alignment, in-place use and errors as for dwp_scan_exclusive.
+ */
+dwp_status dwp_scan_two_level(dwp_op op, dwp_mode mode, const void *d_in, void *d_out, size_t n,
+                              void *d_scratch, size_t *scratch_bytes, dwp_stream stream);
+
+/*
  * Segmented u32 addition reduction over CSR offsets ("GPUSegmentedScan"
  * (luma.gl), section "Composition", which names the segmented reduction
  * beside the segmented scan; the segments are those of "Contract"):

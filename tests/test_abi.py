@@ -174,3 +174,25 @@ def test_segreduce_size_query_and_validation(lib):
     assert R(v, o, nseg, v + 400, n, s, 128, 0)[0] == dwp.DWP_ERR_ALIASING    # out inside values
     assert R(v, o, nseg, o + 8, n, s, 128, 0)[0] == dwp.DWP_ERR_ALIASING      # out over offsets
     assert R(v, o, nseg, out, n, out + 16, 128, 0)[0] == dwp.DWP_ERR_ALIASING  # scratch over out
+
+
+def test_two_level_size_query_and_validation(lib):
+    R = dwp.dwp_scan_two_level
+    assert R(dwp.DWP_U32_ADD, dwp.DWP_EXCLUSIVE, 0, 0, 0, 0, 0, 0) == (dwp.DWP_SUCCESS, 128)
+    assert R(dwp.DWP_U32_ADD, dwp.DWP_EXCLUSIVE, 0, 0, 1, 0, 0, 0) == (dwp.DWP_SUCCESS, 132)
+    assert R(dwp.DWP_U32_ADD, dwp.DWP_EXCLUSIVE, 0, 0, 4096 * 4, 0, 0, 0) == (dwp.DWP_SUCCESS, 144)
+    assert R(dwp.DWP_U32_ADD, dwp.DWP_EXCLUSIVE, 0, 0, 4096 * 4 + 1, 0, 0, 0) == (dwp.DWP_SUCCESS, 148)
+    # never more than the single-pass scan asks for
+    for n in (1, 4096, 4097, 7168, 7169, 12000, 1 << 20, (1 << 26) - 1, 1 << 26):
+        assert R(0, 0, 0, 0, n, 0, 0, 0)[1] <= dwp.dwp_scan_exclusive(0, 0, 0, n, 0, 0, 0)[1], n
+    assert R(dwp.DWP_U32_ADD, dwp.DWP_EXCLUSIVE, 0, 0, 1 << 26, 0, 0, 0) == (dwp.DWP_SUCCESS, 128 + 4 * 16384)
+    assert R(dwp.DWP_U32_ADD, dwp.DWP_EXCLUSIVE, 0, 0, (1 << 26) + 1, 0, 0, 0)[0] == dwp.DWP_ERR_INVALID_VALUE
+    n, need = 1000, 132
+    s = A + (1 << 30)
+    assert R(5, 0, A, A + 8192, n, s, need, 0)[0] == dwp.DWP_ERR_INVALID_VALUE
+    assert R(0, 3, A, A + 8192, n, s, need, 0)[0] == dwp.DWP_ERR_INVALID_VALUE
+    assert R(0, 0, A, A + 8192, n, s, need - 1, 0)[0] == dwp.DWP_ERR_SCRATCH_TOO_SMALL
+    assert R(0, 0, 0, A + 8192, n, s, need, 0)[0] == dwp.DWP_ERR_INVALID_VALUE
+    assert R(0, 0, A + 4, A + 8192, n, s, need, 0)[0] == dwp.DWP_ERR_MISALIGNED
+    assert R(0, 0, A, A + 16, n, s, need, 0)[0] == dwp.DWP_ERR_ALIASING
+    assert R(0, 0, A, A + 8192, n, A + 32, need, 0)[0] == dwp.DWP_ERR_ALIASING
