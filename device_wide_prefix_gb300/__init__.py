@@ -53,7 +53,12 @@ EXPORTS = [
     "dwp_debug_set_fault",
     "dwp_set_lookback_window",
     "dwp_scan_static_scratch",
+    "dwp_read_static_status",
     "dwp_scan_two_level",
+    "dwp_compact_by_flags_staged",
+    "dwp_read_lookback_stats",
+    "dwp_debug_set_delay",
+    "dwp_debug_warp_scan_trace",
 ]
 
 _lib = None
@@ -83,8 +88,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         f.restype = c.c_int
     lib.dwp_segmented_scan_u32.argtypes = [P, P, S, P, S, c.c_int, P, Z, P]
     lib.dwp_segmented_scan_u32.restype = c.c_int
-    lib.dwp_compact_by_flags.argtypes = [P, P, S, P, P, P, Z, P]
-    lib.dwp_compact_by_flags.restype = c.c_int
+    for name in ("dwp_compact_by_flags", "dwp_compact_by_flags_staged"):
+        getattr(lib, name).argtypes = [P, P, S, P, P, P, Z, P]
+        getattr(lib, name).restype = c.c_int
     lib.dwp_linear_recurrence_f32.argtypes = [P, P, P, S, c.c_int, P, Z, P]
     lib.dwp_linear_recurrence_f32.restype = c.c_int
     lib.dwp_segmented_reduce_u32.argtypes = [P, P, S, P, S, P, Z, P]
@@ -93,6 +99,15 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dwp_read_status.restype = c.c_int
     lib.dwp_read_fallbacks.argtypes = [P, P, c.POINTER(c.c_uint32)]
     lib.dwp_read_fallbacks.restype = c.c_int
+    U = c.POINTER(c.c_uint32)
+    lib.dwp_read_lookback_stats.argtypes = [P, P, U, U, U]
+    lib.dwp_read_lookback_stats.restype = c.c_int
+    lib.dwp_read_static_status.argtypes = [P]
+    lib.dwp_read_static_status.restype = c.c_int
+    lib.dwp_debug_set_delay.argtypes = [c.c_uint32, c.c_uint32, c.c_uint32]
+    lib.dwp_debug_set_delay.restype = c.c_int
+    lib.dwp_debug_warp_scan_trace.argtypes = [P, S, P, P]
+    lib.dwp_debug_warp_scan_trace.restype = c.c_int
     lib.dwp_status_string.argtypes = [c.c_int]
     lib.dwp_status_string.restype = c.c_char_p
     lib.dwp_version.argtypes = []
@@ -183,8 +198,43 @@ def dwp_scan_static_scratch(op, mode, d_in, d_out, n, stream) -> int:
                                           stream or None)
 
 
+def dwp_read_static_status(stream) -> int:
+    """dwp.h dwp_read_static_status: device status of the last
+    dwp_scan_static_scratch call on the current device (synchronises)."""
+    return load().dwp_read_static_status(stream or None)
+
+
+def dwp_compact_by_flags_staged(d_records, d_flags, n, d_out, d_count, d_scratch, scratch_bytes,
+                                stream):
+    """dwp.h dwp_compact_by_flags_staged; returns (status, scratch_bytes after the call)."""
+    sb = ctypes.c_size_t(scratch_bytes)
+    st = load().dwp_compact_by_flags_staged(d_records or None, d_flags or None, n, d_out or None,
+                                            d_count or None, d_scratch or None, ctypes.byref(sb),
+                                            stream or None)
+    return st, sb.value
+
+
 def dwp_read_status(d_scratch, stream) -> int:
     return load().dwp_read_status(d_scratch or None, stream or None)
+
+
+def dwp_read_lookback_stats(d_scratch, stream):
+    """(status, fallbacks, intermediates, jumps) of the last call on d_scratch."""
+    a, b, c_ = ctypes.c_uint32(0), ctypes.c_uint32(0), ctypes.c_uint32(0)
+    st = load().dwp_read_lookback_stats(d_scratch or None, stream or None, ctypes.byref(a),
+                                        ctypes.byref(b), ctypes.byref(c_))
+    return st, a.value, b.value, c_.value
+
+
+def dwp_debug_warp_scan_trace(d_x, width, d_steps, stream) -> int:
+    """dwp.h dwp_debug_warp_scan_trace (test hook): the warp Hillis-Steele
+    scan's value per lane after each of its five steps."""
+    return load().dwp_debug_warp_scan_trace(d_x or None, width, d_steps or None, stream or None)
+
+
+def dwp_debug_set_delay(seed: int, fraction_ppm: int, max_ns: int) -> int:
+    """dwp.h dwp_debug_set_delay (test hook): seeded sleeps at publication points."""
+    return load().dwp_debug_set_delay(seed & 0xFFFFFFFF, fraction_ppm, max_ns)
 
 
 def dwp_read_fallbacks(d_scratch, stream):
@@ -436,6 +486,43 @@ def compact_by_flags(records, flags, out=None, count=None, scratch=None, stream=
                                      _stream_of(records, stream))
     _check(st, "dwp_compact_by_flags")
     return out, count
+
+
+def compact_staged_scratch_bytes(n: int) -> int:
+    st, b = dwp_compact_by_flags_staged(None, None, n, None, None, None, 0, None)
+    _check(st, "staged compaction scratch size query")
+    return b
+
+
+def compact_by_flags_staged(records, flags, out=None, count=None, scratch=None, stream=None):
+    """compact_by_flags by the staged three-launch form (flags and offsets
+    written to scratch): the comparison point for the fused kernel."""
+    torch = _torch()
+    n = flags.numel()
+    if not (records.is_cuda and flags.is_cuda and records.is_contiguous() and flags.is_contiguous()):
+        raise ValueError("records and flags must be contiguous CUDA tensors")
+    if records.numel() * records.element_size() != 16 * n or flags.element_size() != 1:
+        raise ValueError("records must hold 16 bytes per flag byte")
+    if out is None:
+        out = torch.empty_like(records)
+    if count is None:
+        count = torch.empty(1, dtype=torch.int32, device=records.device)
+    if scratch is None:
+        scratch = alloc_scratch(compact_staged_scratch_bytes(n), records.device)
+    with torch.cuda.device(records.device):
+        st, _ = dwp_compact_by_flags_staged(records.data_ptr(), flags.data_ptr(), n, out.data_ptr(),
+                                            count.data_ptr(), scratch.data_ptr(), scratch.numel(),
+                                            _stream_of(records, stream))
+    _check(st, "dwp_compact_by_flags_staged")
+    return out, count
+
+
+def read_lookback_stats(scratch, stream=None) -> dict:
+    """Fallbacks, intermediates published and jumps over them in the last
+    call that used `scratch` (synchronises)."""
+    st, fb, im, jp = dwp_read_lookback_stats(scratch.data_ptr(), _stream_of(scratch, stream))
+    _check(st, "dwp_read_lookback_stats")
+    return {"fallbacks": fb, "intermediates": im, "jumps": jp}
 
 
 def read_status(scratch, stream=None) -> int:

@@ -3,6 +3,7 @@
 // argument error never enqueues work.
 #include <cuda_runtime.h>
 
+#include <cstddef>
 #include <cstdint>
 
 #include "launch.h"
@@ -348,6 +349,33 @@ dwp_status dwp_read_fallbacks(const void *d_scratch, dwp_stream stream, uint32_t
 dwp_status dwp_debug_set_fault(uint32_t never_publish_tile, uint32_t spin_limit,
                                uint32_t fallback_polls) {
     set_fault_config(never_publish_tile, spin_limit, fallback_polls);
+    return DWP_SUCCESS;
+}
+
+dwp_status dwp_debug_set_delay(uint32_t seed, uint32_t fraction_ppm, uint32_t max_ns) {
+    if (fraction_ppm > 1000000u || max_ns > kMaxDelayNs) return DWP_ERR_INVALID_VALUE;
+    // a tile sleeps at a point when a 32-bit hash falls below the threshold
+    const uint64_t thr = (uint64_t(fraction_ppm) << 32) / 1000000u;
+    set_delay_config(seed, thr > 0xffffffffull ? 0xffffffffu : uint32_t(thr), max_ns);
+    return DWP_SUCCESS;
+}
+
+dwp_status dwp_read_lookback_stats(const void *d_scratch, dwp_stream stream, uint32_t *fallbacks,
+                                   uint32_t *intermediates, uint32_t *jumps) {
+    if (!d_scratch) return DWP_ERR_INVALID_VALUE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t v[3] = {0u, 0u, 0u};
+    const auto *hdr = reinterpret_cast<const ScratchHeader *>(d_scratch);
+    static_assert(offsetof(ScratchHeader, jumps) == offsetof(ScratchHeader, fallbacks) + 8,
+                  "the three counters are adjacent");
+    if (cudaMemcpyAsync(v, &hdr->fallbacks, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return DWP_ERR_CUDA;
+    }
+    if (fallbacks) *fallbacks = v[0];
+    if (intermediates) *intermediates = v[1];
+    if (jumps) *jumps = v[2];
     return DWP_SUCCESS;
 }
 

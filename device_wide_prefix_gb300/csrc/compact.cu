@@ -215,6 +215,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             if (ld_volatile_smem(sm.abort_flag()) == 0) {
                 t = atomicAdd(&hdr->tile_counter, 1u);
                 if (t >= num_tiles) t = kNoTile;
+                else perturb(fault, t, kSiteDraw);
             }
             *reinterpret_cast<volatile uint32_t *>(sm.tile_id(i)) = t;
             if (t == kNoTile) {
@@ -272,10 +273,13 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             for (int w2 = 0; w2 < NW; ++w2) {
                 const uint32_t c = lane + 32u * w2;
                 uint32_t cnt = 0;
-                if (valid == uint32_t(TILE)) {
+                // straight from the slot wherever all IT flags were
+                // bulk-copied (a ragged last tile too); flag by flag only for
+                // the threads holding the (at most 15) flags after the bulk part
+                if (c * IT + IT <= fbulk) {
 #pragma unroll
                     for (int q = 0; q < IT; ++q) cnt += sf[c * IT + q] != 0;
-                } else {
+                } else if (c * IT < valid) {
                     for (int q = 0; q < IT; ++q) cnt += keep_at(sf, flags, base, c * IT + q, fbulk, valid);
                 }
                 pre[prefix_slot(c)] = cnt;
@@ -300,15 +304,18 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             }
 #pragma unroll
             for (int q = 0; q < PER; ++q) pre[prefix_slot(lane * PER + q)] = lane_excl + mine[q];
+            perturb(fault, t, kSiteAggregate);
             if (lane == 0 && t != fault.never_publish_tile)
                 st_relaxed_gpu(desc + t, make_desc(t == 0 ? kPrefix : kAggregate, total));
             uint32_t carry = 0;
             int rc = 0;
+            perturb(fault, t, kSiteLookback);
             if (t != 0)
                 rc = lookback<Op, C::kLookK>(desc, t, lane, fault.spin_limit, fault.fallback_polls,
-                                             CompactRescue<TILE>{flags, n}, &hdr->fallbacks,
+                                             CompactRescue<TILE>{flags, n}, hdr,
                                              fault.lookback_window, total,
                                              t != fault.never_publish_tile, sm.lb_scratch(i), &carry);
+            if (rc == 0) perturb(fault, t, kSitePrefix);
             if (lane == 0) {
                 if (rc == 0) {
                     if (t != 0 && t != fault.never_publish_tile)

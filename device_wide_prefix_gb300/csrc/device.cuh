@@ -224,6 +224,52 @@ __device__ __forceinline__ void record_error(ScratchHeader *hdr, uint32_t code) 
 }
 
 // ---------------------------------------------------------------------------
+// Schedule perturbation, a test hook (dwp_debug_set_delay).  A missing
+// ordering or synchronisation in a chained scan shows up only under rare
+// interleavings ("Parallel Prefix Sum (Scan), in depth", section "Failure
+// modes"), so a test can make a seeded subset of tiles sleep at their
+// publication points to shuffle the order in which descriptors appear.
+// Whether tile t sleeps at point `site` is decided by a hash of (seed, t,
+// site) below `threshold`; the sleep is a second hash modulo max_ns + 1
+// nanoseconds, timed on %globaltimer, and ends after a bounded number of
+// polls whatever the timer says.  Warp-uniform when every lane passes the
+// same arguments.  Off (threshold 0) it costs one compare.
+
+// MurmurHash3's 32-bit finaliser (Appleby): a bijective avalanche mix.
+__device__ __forceinline__ uint32_t fmix32(uint32_t h) {
+    h ^= h >> 16;
+    h *= 0x85ebca6bu;
+    h ^= h >> 13;
+    h *= 0xc2b2ae35u;
+    h ^= h >> 16;
+    return h;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void perturb(const LaunchKnobs &k, uint32_t t, uint32_t site) {
+    if (k.delay_threshold == 0u) return;
+    const uint32_t h = fmix32(k.delay_seed ^ fmix32(t * 8u + site + 1u));
+    if (h >= k.delay_threshold) return;
+    const uint32_t ns = fmix32(h ^ 0x9e3779b9u) % (k.delay_max_ns + 1u);
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 0; i < 4096u && global_ns() - t0 < ns; ++i) __nanosleep(32);
+}
+
+// Perturbation points.
+enum : uint32_t {
+    kSiteDraw = 0u,       // after a tile index is drawn, before its load
+    kSiteAggregate = 1u,  // before the aggregate is published
+    kSiteLookback = 2u,   // before the look-back starts
+    kSitePrefix = 3u,     // before the inclusive prefix is published
+    kSiteMidWord = 4u     // between the two words of a two-word descriptor
+};
+
+// ---------------------------------------------------------------------------
 // Tile descriptor ("Single-Pass Prefix Scan with Decoupled Look-Back",
 // "Three states in a per-block descriptor"): state in the high 32 bits,
 // 32-bit payload in the low 32 bits.  POISON marks a tile whose chain was
@@ -324,7 +370,7 @@ __device__ __forceinline__ uint32_t warp_lower_bound(const uint32_t *off, uint32
 // against the invalid state.  So of several rescuers and the tile's own
 // block, whichever writes first wins, and a lost swap hands back the winning
 // descriptor (the same value for the integer operators; for f32 another
-// grouping of the same sum).  Each swap won adds one to *fallbacks.  The
+// grouping of the same sum).  Each swap won adds one to hdr->fallbacks.  The
 // input must stay unmodified for the whole launch: callers disable the
 // fallback (fallback_polls = 0) for an in-place scan.
 //
@@ -335,7 +381,8 @@ __device__ __forceinline__ uint32_t warp_lower_bound(const uint32_t *off, uint32
 // combination of everything folded so far with t's own aggregate `own`, and
 // the number d of tiles it covers (t - d + 1 .. t), as state kSpan0 + d.  A
 // look-back that meets an intermediate as the nearest stop of its window
-// folds it and jumps d tiles back at once.  Folds happen a window of K*32
+// folds it and jumps d tiles back at once.  Publications and jumps are
+// counted in hdr->intermediates and hdr->jumps.  Folds happen a window of K*32
 // tiles at a time, so the effective window is a multiple of K*32.  A tile
 // that has already published its prefix must pass publish = false.
 //
@@ -345,7 +392,7 @@ __device__ __forceinline__ uint32_t warp_lower_bound(const uint32_t *off, uint32
 template <class Op, int K, class Rescue>
 __device__ __forceinline__ int lookback(uint64_t *desc, uint32_t t, uint32_t lane,
                                         uint32_t spin_limit, uint32_t fallback_polls,
-                                        const Rescue &rescue, uint32_t *fallbacks,
+                                        const Rescue &rescue, ScratchHeader *hdr,
                                         uint32_t window, uint32_t own, bool publish,
                                         uint32_t *scratch, typename Op::T *carry_out) {
     using T = typename Op::T;
@@ -400,7 +447,7 @@ __device__ __forceinline__ int lookback(uint64_t *desc, uint32_t t, uint32_t lan
                                 reinterpret_cast<unsigned long long *>(desc + p), 0ull,
                                 static_cast<unsigned long long>(mine));
                             got = old == 0ull ? static_cast<unsigned long long>(mine) : old;
-                            if (old == 0ull) atomicAdd(fallbacks, 1u);
+                            if (old == 0ull) atomicAdd(&hdr->fallbacks, 1u);
                         }
                         got = __shfl_sync(0xffffffffu, got, 0);
                         if (lane == j) d[i] = got;
@@ -428,13 +475,16 @@ __device__ __forceinline__ int lookback(uint64_t *desc, uint32_t t, uint32_t lan
         }
         carry = Op::combine(Op::warp_reduce(acc, lane, scratch), carry);
         if (kind == 0u) break;
+        if (kind == 2u && lane == 0) atomicAdd(&hdr->jumps, 1u);
         // the intermediate at position `last` covers `span` tiles ending at it
         base -= kind == 2u ? int64_t(last) + int64_t(__reduce_max_sync(0xffffffffu, span)) : 32 * K;
         const uint64_t folded = uint64_t(int64_t(t) - 1 - base);
         if (window != 0u && publish && folded >= next_pub) {
-            if (lane == 0)
+            if (lane == 0) {
                 st_relaxed_gpu(desc + t, make_desc(kSpan0 + uint32_t(folded) + 1u,
                                                    Op::to_bits(Op::combine(carry, Op::from_bits(own)))));
+                atomicAdd(&hdr->intermediates, 1u);
+            }
             next_pub = folded + window;
         }
     }

@@ -17,6 +17,9 @@ std::atomic<uint32_t> g_never_publish{0xffffffffu};
 std::atomic<uint32_t> g_spin_limit{0u};
 std::atomic<uint32_t> g_fallback_polls{0u};
 std::atomic<uint32_t> g_lookback_window{0u};
+std::atomic<uint32_t> g_delay_seed{0u};
+std::atomic<uint32_t> g_delay_threshold{0u};
+std::atomic<uint32_t> g_delay_max_ns{0u};
 }  // namespace
 
 int device_blocks(const void *kernel, int threads, size_t smem_bytes) {
@@ -48,7 +51,16 @@ LaunchKnobs current_launch_knobs() {
     const uint32_t fb = g_fallback_polls.load();
     f.fallback_polls = fb == 0u ? kDefaultFallbackPolls : (fb == 0xffffffffu ? 0u : fb);
     f.lookback_window = g_lookback_window.load();
+    f.delay_seed = g_delay_seed.load();
+    f.delay_threshold = g_delay_threshold.load();
+    f.delay_max_ns = g_delay_max_ns.load();
     return f;
+}
+
+void set_delay_config(uint32_t seed, uint32_t threshold, uint32_t max_ns) {
+    g_delay_seed.store(seed);
+    g_delay_max_ns.store(max_ns);
+    g_delay_threshold.store(threshold);
 }
 
 void set_lookback_window(uint32_t tiles) { g_lookback_window.store(tiles); }

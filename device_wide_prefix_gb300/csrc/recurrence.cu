@@ -382,6 +382,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 if (ld_volatile_smem(sm.abort_flag()) == 0) {
                     t = atomicAdd(&hdr->tile_counter, 1u);
                     if (t >= num_tiles) t = kNoTile;
+                    else perturb(fault, t, kSiteDraw);
                 }
                 *reinterpret_cast<volatile uint32_t *>(sm.tile_id(gi)) = t;
                 ++taken;
@@ -463,7 +464,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             for (int w2 = 0; w2 < NW; ++w2) {
                 const uint32_t c = lane + 32u * w2;
                 float A = 1.0f, B = 0.0f;
-                if (valid == uint32_t(TILE)) {
+                // vectors wherever the thread's items are all bulk-copied (a
+                // ragged last tile too), element by element only for the
+                // thread holding the 1-3 elements after the bulk part; a
+                // thread past the end keeps the identity map
+                if (c * ITEMS + ITEMS <= bulk) {
                     const float4 *a4 = reinterpret_cast<const float4 *>(sa) + c * (ITEMS / 4);
                     const float4 *b4 = reinterpret_cast<const float4 *>(sb) + c * (ITEMS / 4);
 #pragma unroll
@@ -475,7 +480,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                         B = __fmaf_rn(qa.w, B, qb.w);
                         A = __fmul_rn(__fmul_rn(__fmul_rn(qa.w, qa.z), __fmul_rn(qa.y, qa.x)), A);
                     }
-                } else {
+                } else if (c * ITEMS < valid) {
                     for (int j = 0; j < ITEMS; ++j) {
                         float av, bv;
                         rec_elem(sa, sb, ga, gb, base, c * ITEMS + j, bulk, valid, av, bv);
@@ -527,12 +532,14 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 pa[prefix_slot(lane * PER + j)] = __fmul_rn(mA[j], eA);
                 pb[prefix_slot(lane * PER + j)] = __fmaf_rn(mA[j], eB, mB[j]);
             }
+            perturb(fault, t, kSiteAggregate);
             if (lane == 0) {
                 if (t != fault.never_publish_tile) {
                     if (t == 0) {
                         st_relaxed_gpu(desc + 1, make_desc(kPrefix, __float_as_uint(gB)));
                     } else {
                         st_relaxed_gpu(desc + 2 * uint64_t(t), make_desc(kAggregate, __float_as_uint(gA)));
+                        perturb(fault, t, kSiteMidWord);
                         st_relaxed_gpu(desc + 2 * uint64_t(t) + 1,
                                        make_desc(kAggregate, __float_as_uint(gB)));
                     }
@@ -567,9 +574,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             if (!draining && ld_volatile_smem(sm.abort_flag()) != 0) draining = true;
             float carry = 0.0f;
             int rc = (draining || ld_volatile_smem(sm.lbres(i)) != 0u) ? 1 : 0;
+            if (rc == 0) perturb(fault, t, kSiteLookback);
             if (rc == 0 && t != 0)
                 rc = lookback_affine(desc, t, lane, fault.spin_limit, fault.fallback_polls, rescue,
                                      &hdr->fallbacks, scr, &carry);
+            if (rc == 0) perturb(fault, t, kSitePrefix);
             if (lane == 0) {
                 if (rc == 0) {
                     if (t != 0 && t != fault.never_publish_tile)
@@ -663,7 +672,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         float h = __fmaf_rn(sm.pre_a(i)[prefix_slot(c)], *sm.carry(i), sm.pre_b(i)[prefix_slot(c)]);
         __syncwarp();
         if (lane == 0) mbar_arrive(sm.info_free(i));
-        if (valid == uint32_t(TILE)) {
+        if (p0 + ITEMS <= bulk) {
             const float4 *a4 = reinterpret_cast<const float4 *>(sa + p0);
             float4 *b4 = reinterpret_cast<float4 *>(sb + p0);
 #pragma unroll
@@ -683,7 +692,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 }
                 b4[v] = r;
             }
-        } else {
+        } else if (p0 < valid) {
             for (int jj = 0; jj < ITEMS; ++jj) {
                 const uint32_t pos = p0 + jj;
                 float av, bv;

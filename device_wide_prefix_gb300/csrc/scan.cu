@@ -273,6 +273,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 if (ld_volatile_smem(sm.abort_flag()) == 0) {
                     t = atomicAdd(&hdr->tile_counter, 1u);
                     if (t >= num_tiles) t = kNoTile;
+                    else perturb(fault, t, kSiteDraw);
                 }
                 *reinterpret_cast<volatile uint32_t *>(sm.tile_id(gi)) = t;
                 ++taken;
@@ -349,31 +350,30 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             uint32_t *pre = sm.prefix(i);
             uint32_t *lt = sm.lane_tot(s);
             // totals of consumer threads c = lane + 32*w, whose ITEMS
-            // contiguous elements start at c*ITEMS
+            // contiguous elements start at c*ITEMS.  A thread whose items
+            // all lie in the bulk-copied part reads them as 16-byte vectors
+            // (in a ragged last tile too); only the one thread that holds
+            // the last 1-3 elements past the bulk part reads element by
+            // element, and threads wholly past the end contribute nothing.
             T tot[NW];
-            if (valid == uint32_t(TILE)) {
-                const uint4 *v4 = reinterpret_cast<const uint4 *>(buf);
+            const uint4 *v4 = reinterpret_cast<const uint4 *>(buf);
 #pragma unroll
-                for (int w2 = 0; w2 < NW; ++w2) {
-                    const uint32_t c = lane + 32u * w2;
-                    T acc = Op::identity();
+            for (int w2 = 0; w2 < NW; ++w2) {
+                const uint32_t c = lane + 32u * w2;
+                const uint32_t p0 = c * ITEMS;
+                T acc = Op::identity();
+                if (p0 + ITEMS <= bulk) {
 #pragma unroll
                     for (int v = 0; v < ITEMS / 4; ++v) {
                         const uint4 q = v4[c * (ITEMS / 4) + v];
                         acc = Op::combine(acc, Op::combine(Op::combine(Op::from_bits(q.x), Op::from_bits(q.y)),
                                                            Op::combine(Op::from_bits(q.z), Op::from_bits(q.w))));
                     }
-                    tot[w2] = acc;
-                }
-            } else {
-#pragma unroll
-                for (int w2 = 0; w2 < NW; ++w2) {
-                    const uint32_t c = lane + 32u * w2;
-                    T acc = Op::identity();
+                } else if (p0 < valid) {
                     for (int j = 0; j < ITEMS; ++j)
-                        acc = Op::combine(acc, tile_elem<Op>(buf, in, base, c * ITEMS + j, bulk, valid));
-                    tot[w2] = acc;
+                        acc = Op::combine(acc, tile_elem<Op>(buf, in, base, p0 + j, bulk, valid));
                 }
+                tot[w2] = acc;
             }
             // the input stage is no longer needed
             __syncwarp();
@@ -406,6 +406,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             for (int j = 0; j < PER; ++j)
                 pre[prefix_slot(lane * PER + j)] = Op::to_bits(Op::combine(lane_excl, mine[j]));
             // publish the aggregate at once (tile 0: its inclusive prefix)
+            perturb(fault, t, kSiteAggregate);
             if (lane == 0) {
                 if (t != fault.never_publish_tile)
                     st_relaxed_gpu(desc + t, make_desc(t == 0 ? kPrefix : kAggregate, Op::to_bits(agg)));
@@ -436,12 +437,14 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             if (!draining && ld_volatile_smem(sm.abort_flag()) != 0) draining = true;
             T carry = Op::identity();
             int rc = (draining || ld_volatile_smem(sm.lbres(i)) != 0u) ? 1 : 0;
+            if (rc == 0) perturb(fault, t, kSiteLookback);
             if (rc == 0 && t != 0)
                 rc = lookback<Op, C::kLookK>(desc, t, lane, fault.spin_limit, fault.fallback_polls,
-                                             ScanRescue<Op, TILE>{in, n}, &hdr->fallbacks,
+                                             ScanRescue<Op, TILE>{in, n}, hdr,
                                              fault.lookback_window, *sm.agg(i),
                                              t != fault.never_publish_tile, sm.lb_scratch(int(j)),
                                              &carry);
+            if (rc == 0) perturb(fault, t, kSitePrefix);
             if (lane == 0) {
                 if (rc == 0) {
                     if (t != 0 && t != fault.never_publish_tile)
@@ -535,7 +538,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         T acc = Op::combine(Op::from_bits(*sm.carry(i)), Op::from_bits(sm.prefix(i)[prefix_slot(c)]));
         __syncwarp();
         if (lane == 0) mbar_arrive(sm.info_free(i));  // the info slot has been read
-        if (valid == uint32_t(TILE)) {
+        // as in the reduce: vectors wherever the thread's items are all in
+        // the bulk part, element by element only for the thread holding the
+        // ragged 1-3 elements after it, nothing past the end
+        if (p0 + ITEMS <= bulk) {
             uint4 *v4 = reinterpret_cast<uint4 *>(buf + p0);
 #pragma unroll
             for (int v = 0; v < ITEMS / 4; ++v) {
@@ -555,7 +561,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 }
                 v4[v] = make_uint4(r[0], r[1], r[2], r[3]);
             }
-        } else {
+        } else if (p0 < valid) {
             for (int j = 0; j < ITEMS; ++j) {
                 const uint32_t pos = p0 + j;
                 const T xv = tile_elem<Op>(buf, in, base, pos, bulk, valid);

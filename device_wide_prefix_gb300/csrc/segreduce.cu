@@ -134,6 +134,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 
         if (!__all_sync(0xffffffffu, mbar_wait(sm.full(j), (it >> 1) & 1u, kPipeWaitLimit))) {
             if (lane == 0) record_error(hdr, DWP_ERR_PIPELINE_TIMEOUT);
+            // Drain before the block retires: this copy and the one already
+            // started into the other stage may still be writing shared
+            // memory.  Each wait is bounded; after that the warp leaves.
+            mbar_wait(sm.full(j), (it >> 1) & 1u, kPipeWaitLimit);
+            if (next != kNoTile) mbar_wait(sm.full(j ^ 1), ((it + 1) >> 1) & 1u, kPipeWaitLimit);
             return;
         }
         const uint32_t *buf = sm.stage(j);

@@ -287,6 +287,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 if (ld_volatile_smem(sm.abort_flag()) == 0) {
                     t = atomicAdd(&hdr->tile_counter, 1u);
                     if (t >= num_tiles) t = kNoTile;
+                    else perturb(fault, t, kSiteDraw);
                 }
                 *reinterpret_cast<volatile uint32_t *>(sm.tile_id(gi)) = t;
                 ++taken;
@@ -414,14 +415,19 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 const uint32_t c = lane + 32u * w2;
                 const uint32_t hb = tile_heads ? head_bits(heads, c * ITEMS, ITEMS) : 0u;
                 uint32_t acc = 0;
-                if (valid == uint32_t(TILE) && !hb) {
+                // vectors wherever the thread's items are all bulk-copied (a
+                // ragged last tile too); element by element only for the
+                // thread holding the 1-3 elements after the bulk part; heads
+                // lie below the tile end, so threads past it hold nothing
+                const bool vec = c * ITEMS + ITEMS <= bulk;
+                if (vec && !hb) {
                     const uint4 *v4 = reinterpret_cast<const uint4 *>(buf);
 #pragma unroll
                     for (int v = 0; v < ITEMS / 4; ++v) {
                         const uint4 q = v4[c * (ITEMS / 4) + v];
                         acc += (q.x + q.y) + (q.z + q.w);
                     }
-                } else if (valid == uint32_t(TILE)) {
+                } else if (vec) {
                     const uint4 *v4 = reinterpret_cast<const uint4 *>(buf);
                     // only the items from the last head on count
                     const int from = hb ? 31 - __clz(hb) : 0;
@@ -433,7 +439,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                         for (int e = 0; e < 4; ++e)
                             if (4 * v + e >= from) acc += qq[e];
                     }
-                } else {
+                } else if (c * ITEMS < valid) {
                     for (int j = 0; j < ITEMS; ++j) {
                         const uint32_t x = seg_elem(buf, in, base, c * ITEMS + j, bulk, valid);
                         acc = ((hb >> j) & 1u) ? x : acc + x;
@@ -489,6 +495,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 pre[prefix_slot(lane * PER + j)] = hj ? mv[j] : ev + mv[j];
                 if (tile_heads) ph[lane * PER + j] = (hj | eh) ? 1 : 0;
             }
+            perturb(fault, t, kSiteAggregate);
             if (lane == 0) {
                 if (t != fault.never_publish_tile)
                     st_relaxed_gpu(desc + t, make_desc((t == 0 || ah) ? kPrefix : kAggregate, av));
@@ -524,12 +531,14 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             uint32_t carry = 0;
             int rc = (draining || ld_volatile_smem(sm.lbres(i)) != 0u) ? 1 : 0;
             const bool ah = ld_volatile_smem(sm.agg_head(i)) != 0u;
+            if (rc == 0) perturb(fault, t, kSiteLookback);
             if (rc == 0 && t != 0 && ld_volatile_smem(sm.first_head(i)) == 0u)
                 rc = lookback<Op, C::kLookK>(desc, t, lane, fault.spin_limit, fault.fallback_polls,
                                              SegRescue{in, off, nseg, n, uint32_t(TILE)},
-                                             &hdr->fallbacks, fault.lookback_window, *sm.agg(i),
+                                             hdr, fault.lookback_window, *sm.agg(i),
                                              !ah && t != fault.never_publish_tile, sm.lb_scratch(i),
                                              &carry);
+            if (rc == 0) perturb(fault, t, kSitePrefix);
             if (lane == 0) {
                 if (rc == 0) {
                     if (t != 0 && !ah && t != fault.never_publish_tile)
@@ -627,7 +636,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         uint32_t acc = phd ? pv : *sm.carry(i) + pv;
         __syncwarp();
         if (lane == 0) mbar_arrive(sm.info_free(i));  // the info slot has been read
-        if (valid == uint32_t(TILE) && covered) {
+        if (covered && p0 + ITEMS <= bulk) {
             uint4 *v4 = reinterpret_cast<uint4 *>(buf + p0);
 #pragma unroll
             for (int v = 0; v < ITEMS / 4; ++v) {
@@ -647,7 +656,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 }
                 v4[v] = make_uint4(r[0], r[1], r[2], r[3]);
             }
-        } else {
+        } else if (p0 < valid) {
             for (int j = 0; j < ITEMS; ++j) {
                 const uint32_t pos = p0 + j;
                 const uint32_t x = seg_elem(buf, in, base, pos, bulk, valid);

@@ -10,8 +10,6 @@
 // it until the process exits, and no call allocates or frees anything.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "launch.h"
 
 namespace {
@@ -27,28 +25,23 @@ static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBy
 
 // In host code `g_static_scratch` names a host-side stand-in, not device
 // memory, so the kernels get the address that cudaGetSymbolAddress returns
-// for the current device, looked up once per device.
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void *g_device_addr[kMaxDevices];
-
+// for the current device.  It is looked up on every call rather than cached:
+// after cudaDeviceReset (or any reset of the primary context) the module is
+// loaded again and the array may sit at another address, and a cached
+// address would then point at memory this library no longer owns.  The
+// lookup is a host-side table query, small next to a scan.
 dwp_status static_scratch_address(void **out) {
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
         cudaGetLastError();
         return DWP_ERR_NO_DEVICE;
     }
-    if (dev < 0 || dev >= kMaxDevices) return DWP_ERR_NO_DEVICE;
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_device_addr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) {
-            cudaGetLastError();
-            return DWP_ERR_CUDA;
-        }
-        g_device_addr[dev] = p;
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) {
+        cudaGetLastError();
+        return DWP_ERR_CUDA;
     }
-    *out = g_device_addr[dev];
+    *out = p;
     return DWP_SUCCESS;
 }
 
@@ -71,4 +64,11 @@ extern "C" dwp_status dwp_scan_static_scratch(dwp_op op, dwp_mode mode, const vo
     size_t bytes = kStaticScratchBytes;
     return m == DWP_INCLUSIVE ? dwp_scan_inclusive(op, d_in, d_out, n, scratch, &bytes, stream)
                               : dwp_scan_exclusive(op, d_in, d_out, n, scratch, &bytes, stream);
+}
+
+extern "C" dwp_status dwp_read_static_status(dwp_stream stream) {
+    void *scratch = nullptr;
+    const dwp_status st = static_scratch_address(&scratch);
+    if (st != DWP_SUCCESS) return st;
+    return dwp_read_status(scratch, stream);
 }

@@ -1,9 +1,10 @@
 // Two-level (reduce, then scan) plain scan in three launches, for sm_103a.
 //
 // "Single-Pass Prefix Scan with Decoupled Look-Back", sections "The
-// two-level decomposition" and "When not to use it": the form the
-// single-pass scan replaces, kept for small inputs, where it "has no
-// spinning and no descriptors" and its extra launches cost microseconds.
+// two-level decomposition" and "When not to use it": the older form that
+// the single-pass scan improves on.  It needs neither descriptors nor any
+// waiting on other blocks, and its two extra launches cost a few
+// microseconds, so it stays useful for small inputs and as a comparison.
 //   1. tl_reduce      block b reduces its chunk of CHUNK elements to one
 //                     total, written to totals[b];
 //   2. tl_scan_totals one block turns the totals into their exclusive scan,
@@ -30,14 +31,35 @@ constexpr int kTlTotThreads = 1024;               // the one block of step 2
 constexpr int kTlTotItems = 16;                   // totals per thread in step 2
 constexpr uint64_t kTlMaxBlocks = uint64_t(kTlTotThreads) * kTlTotItems;
 
+// Inclusive Hillis-Steele scan of one value per lane ("Parallel Prefix Sum
+// (Scan), in depth", section "Hillis-Steele: short span, too much work"):
+// at step d = 1, 2, 4, 8, 16 every lane at or above d combines the value d
+// lanes below it into its own.  With `steps` non-null, lane l also writes
+// its value after step k (d = 2^k) to steps[32k + l], so a test can compare
+// each step with the page's printed trace.
 template <class Op>
-__device__ __forceinline__ typename Op::T warp_incl_scan(typename Op::T v, uint32_t lane) {
+__device__ __forceinline__ typename Op::T warp_incl_scan(typename Op::T v, uint32_t lane,
+                                                        uint32_t *steps = nullptr) {
 #pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
+    for (int d = 1, k = 0; d < 32; d <<= 1, ++k) {
         const typename Op::T u = __shfl_up_sync(0xffffffffu, v, d);
         if (lane >= uint32_t(d)) v = Op::combine(u, v);
+        if (steps) steps[32 * k + lane] = Op::to_bits(v);
     }
     return v;
+}
+
+// One warp runs warp_incl_scan over x[0 .. width) (the identity in the
+// lanes past width) and writes the value of lanes 0 .. width-1 after each
+// of the five steps to out[width * k + l].
+__global__ void warp_scan_trace_kernel(const uint32_t *x, uint32_t width, uint32_t *out) {
+    __shared__ uint32_t steps[5 * 32];
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t v = lane < width ? x[lane] : OpU32Add::identity();
+    warp_incl_scan<OpU32Add>(v, lane, steps);
+    __syncwarp();
+    for (uint32_t k = 0; k < 5; ++k)
+        if (lane < width) out[width * k + lane] = steps[32 * k + lane];
 }
 
 // Exclusive scan of one value per thread over the block, in thread order;
@@ -195,3 +217,12 @@ cudaError_t launch_two_level(dwp_op op, bool inclusive, const void *in, void *ou
 }
 
 }  // namespace dwp
+
+extern "C" dwp_status dwp_debug_warp_scan_trace(const uint32_t *d_x, size_t width, uint32_t *d_steps,
+                                                dwp_stream stream) {
+    if (width == 0 || width > 32 || !d_x || !d_steps) return DWP_ERR_INVALID_VALUE;
+    dwp::warp_scan_trace_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        d_x, uint32_t(width), d_steps);
+    if (cudaGetLastError() != cudaSuccess) return DWP_ERR_CUDA;
+    return DWP_SUCCESS;
+}

@@ -171,19 +171,28 @@ dwp_status dwp_compact_by_flags(const void *d_records, const uint8_t *d_flags, s
  *   mode      DWP_EXCLUSIVE or DWP_INCLUSIVE.
  *   n         0 <= n <= DWP_SCAN_STATIC_MAX_N (2^28 elements); a larger n
  *             returns DWP_ERR_SCRATCH_TOO_SMALL before anything is enqueued.
- * The first call on a device looks up that device's address of the array
- * (cudaGetSymbolAddress, with the device current); make that first call
- * before any stream capture.  Every call on a device shares the one array,
- * and each call clears the part it uses on `stream` first, so calls must be
- * ordered on the GPU: two calls that overlap on the GPU (different streams,
- * not synchronised) race and give wrong results.  Device-side timeouts are
- * recorded in the array's status word, which dwp_read_status cannot reach:
- * this entry point does not report them.  DWP_ERR_NO_DEVICE if there is no
- * current device; otherwise the errors of dwp_scan_exclusive.
+ * Every call looks up the current device's address of the array
+ * (cudaGetSymbolAddress), so the address stays right after a device or
+ * context reset.  The first call on a device also loads the library's
+ * device code there: make that first call before any stream capture.  Every
+ * call on a device shares the one array, and each call clears the part it
+ * uses on `stream` first, so calls must be ordered on the GPU: two calls
+ * that overlap on the GPU (different streams, not synchronised) race and
+ * give wrong results.  Device-side timeouts are recorded in the array's
+ * status word: read it with dwp_read_static_status.  DWP_ERR_NO_DEVICE if
+ * there is no current device; otherwise the errors of dwp_scan_exclusive.
  */
 #define DWP_SCAN_STATIC_MAX_N 268435456u
 dwp_status dwp_scan_static_scratch(dwp_op op, dwp_mode mode, const void *d_in, void *d_out,
                                    size_t n, dwp_stream stream);
+
+/*
+ * Device-side status of the most recent dwp_scan_static_scratch call on the
+ * current device: what dwp_read_status returns for a caller-owned scratch
+ * buffer, read from the built-in array.  Synchronises `stream` (order it
+ * after the call).  Copies into host memory only; allocates nothing.
+ */
+dwp_status dwp_read_static_status(dwp_stream stream);
 
 /*
  * The same scans as dwp_scan_exclusive / dwp_scan_inclusive (`mode` picks
@@ -201,6 +210,29 @@ dwp_status dwp_scan_static_scratch(dwp_op op, dwp_mode mode, const void *d_in, v
  */
 dwp_status dwp_scan_two_level(dwp_op op, dwp_mode mode, const void *d_in, void *d_out, size_t n,
                               void *d_scratch, size_t *scratch_bytes, dwp_stream stream);
+
+/*
+ * Stable compaction in three stages, for comparison with the fused
+ * dwp_compact_by_flags ("Prefix scans and compaction", section "Worked
+ * example: Stable stream compaction": compare an implementation that
+ * materialises the flags and their prefixes with a fused one; section
+ * "Common errors": the cost of materialising predicates and prefixes).
+ * Same arguments, output and count as dwp_compact_by_flags; the output is
+ * bit for bit the same.  The stages, in three launches plus the scan's
+ * scratch clear: u32 flags f[i] = (d_flags[i] != 0) written to scratch;
+ * dwp_scan_exclusive of f into offsets in scratch; a scatter that reads f,
+ * the offsets and each kept record and writes it to its slot.  Memory
+ * traffic is about 21 bytes per record plus the kept records' sectors and
+ * output, against 17 plus the output for the fused kernel.
+ *   d_scratch  NULL: *scratch_bytes receives the size needed (the scan's
+ *              scratch plus 8 bytes per record).  Otherwise at least that
+ *              many bytes, 16-byte aligned, overlapping no other argument;
+ *              dwp_read_status on it reports the scan's device status.
+ * Errors as for dwp_compact_by_flags.
+ */
+dwp_status dwp_compact_by_flags_staged(const void *d_records, const uint8_t *d_flags, size_t n,
+                                       void *d_out, uint32_t *d_count, void *d_scratch,
+                                       size_t *scratch_bytes, dwp_stream stream);
 
 /*
  * Segmented u32 addition reduction over CSR offsets ("GPUSegmentedScan"
@@ -272,6 +304,19 @@ dwp_status dwp_read_status(const void *d_scratch, dwp_stream stream);
  */
 dwp_status dwp_read_fallbacks(const void *d_scratch, dwp_stream stream, uint32_t *count);
 
+/*
+ * Look-back counters of the most recent call that used d_scratch (plain
+ * scan, segmented scan or compaction): Decoupled Fallbacks won (as
+ * dwp_read_fallbacks), intermediate descriptors published by a bounded
+ * look-back window ("Single-Pass Prefix Scan with Decoupled Look-Back",
+ * section "Why the work stays linear"; see dwp_set_lookback_window), and
+ * look-back steps that jumped over such an intermediate.  Any output pointer
+ * may be NULL.  Synchronises `stream`.  DWP_ERR_INVALID_VALUE for a NULL
+ * d_scratch; DWP_ERR_CUDA if the synchronisation or the read fails.
+ */
+dwp_status dwp_read_lookback_stats(const void *d_scratch, dwp_stream stream, uint32_t *fallbacks,
+                                   uint32_t *intermediates, uint32_t *jumps);
+
 /* Static, NUL-terminated name of a status code. */
 const char *dwp_status_string(dwp_status status);
 
@@ -314,6 +359,42 @@ dwp_status dwp_set_lookback_window(uint32_t tiles);
  */
 dwp_status dwp_debug_set_fault(uint32_t never_publish_tile, uint32_t spin_limit,
                                uint32_t fallback_polls);
+
+/*
+ * Test hook, not for production use: the step-by-step trace of the warp
+ * layer's Hillis-Steele scan ("Parallel Prefix Sum (Scan), in depth",
+ * section "Hillis-Steele: short span, too much work"), the shuffle scan that
+ * dwp_scan_two_level runs on every warp.  One warp loads d_x[0 .. width)
+ * (u32 addition; lanes past width hold 0) and runs the scan; after step k
+ * (k = 0..4, offset d = 2^k) lane l writes its running value to
+ * d_steps[width * k + l] for l < width.  So the page's 8-element trace can
+ * be checked step by step on the device.
+ *   d_x      device uint32[width];   d_steps  device uint32[5 * width]
+ *   width    1 .. 32 (DWP_ERR_INVALID_VALUE otherwise, or for NULL pointers)
+ * Asynchronous on `stream`; DWP_ERR_CUDA if the launch fails.
+ */
+dwp_status dwp_debug_warp_scan_trace(const uint32_t *d_x, size_t width, uint32_t *d_steps,
+                                     dwp_stream stream);
+
+/*
+ * Test hook, not for production use: schedule perturbation for every later
+ * call of the look-back kernels (plain and segmented scan, compaction,
+ * linear recurrence) in this process until reset.  A missing ordering step
+ * in a chained scan shows only under rare interleavings ("Parallel Prefix
+ * Sum (Scan), in depth", section "Failure modes"); this makes a seeded
+ * subset of tiles sleep at their publication points (after drawing the
+ * tile index, before publishing the aggregate, before the look-back, before
+ * publishing the prefix, and between the two words of a two-word
+ * descriptor), so that descriptors appear in other orders than the
+ * hardware's usual one.  Results must not change.
+ *   seed          selects the subset and the sleep lengths
+ *   fraction_ppm  share of (tile, point) pairs that sleep, in parts per
+ *                 million (0 switches the hook off; at most 1000000)
+ *   max_ns        longest sleep, at most 100000 ns
+ * Every sleep is bounded.  DWP_ERR_INVALID_VALUE for arguments out of
+ * range.  Not thread-safe; affects every device.
+ */
+dwp_status dwp_debug_set_delay(uint32_t seed, uint32_t fraction_ppm, uint32_t max_ns);
 
 #ifdef __cplusplus
 }

@@ -254,7 +254,8 @@ def test_bounded_window_same_result(ref, window, op, inclusive):
     """A bounded look-back window publishes intermediates and jumps over them;
     the output is the oracle's either way.  A silent tile rescued after 64
     polls makes every tile behind it fold a long chain of aggregates, so the
-    intermediates are really published and followed."""
+    intermediates are really published and followed: the scratch header's
+    counters must show both."""
     n = 3000 * tile() + 77
     x = synth.f32_values(n, 31) if op == "f32_add" else synth.u32_full_values(n, 31)
     t = torch.from_numpy(x.view(np.float32 if op == "f32_add" else np.int32)).cuda()
@@ -265,7 +266,12 @@ def test_bounded_window_same_result(ref, window, op, inclusive):
             dwp.dwp_debug_set_fault(silent, 0, 64)
             y = (dwp.scan_inclusive if inclusive else dwp.scan_exclusive)(t, op, scratch=scratch)
             assert dwp.read_status(scratch) == dwp.DWP_SUCCESS
+            stats = dwp.read_lookback_stats(scratch)
             check(ref, x, op, inclusive, y.cpu().numpy().view(x.dtype))
+            if silent != 0xFFFFFFFF:
+                # the tiles queued behind the silent one fold long chains:
+                # they publish intermediates, and later look-backs jump them
+                assert stats["intermediates"] > 0 and stats["jumps"] > 0, stats
     finally:
         dwp.dwp_set_lookback_window(0)
         dwp.dwp_debug_set_fault(0xFFFFFFFF, 0, 0)

@@ -3,6 +3,7 @@ integers bit for bit, f32 within 1e-4 * sum|x| + 1e-6."""
 import numpy as np
 import pytest
 
+import golden_io
 import oracle
 import synth
 
@@ -65,3 +66,27 @@ def test_too_large_is_rejected():
     st, _ = dwp.dwp_scan_two_level(dwp.DWP_U32_ADD, dwp.DWP_EXCLUSIVE, None, None, (1 << 26) + 1,
                                    None, 0, None)
     assert st == dwp.DWP_ERR_INVALID_VALUE
+
+
+def test_warp_hillis_steele_steps_match_the_printed_trace():
+    """The page's 8-element Hillis-Steele trace, step by step, on the warp
+    scan the two-level kernels run: after d = 1, 2, 4 the eight lanes hold
+    the printed rows; the steps d = 8, 16 change nothing in them (they only
+    pull from lanes 8 and up, which hold the identity)."""
+    ex = golden_io.load()["hillis_steele_8"]
+    x = torch.tensor(ex["x"], dtype=torch.int32, device="cuda")
+    steps = torch.full((5 * 8,), -1, dtype=torch.int32, device="cuda")
+    st = dwp.dwp_debug_warp_scan_trace(x.data_ptr(), 8, steps.data_ptr(),
+                                       torch.cuda.current_stream().cuda_stream)
+    assert st == dwp.DWP_SUCCESS
+    rows = steps.view(5, 8).cpu().tolist()
+    assert rows[0] == ex["step_d1"]
+    assert rows[1] == ex["step_d2"]
+    assert rows[2] == ex["step_d4"]
+    assert rows[3] == ex["inclusive"] and rows[4] == ex["inclusive"]
+
+
+def test_warp_scan_trace_rejects_bad_widths():
+    x = torch.zeros(32, dtype=torch.int32, device="cuda")
+    assert dwp.dwp_debug_warp_scan_trace(x.data_ptr(), 0, x.data_ptr(), 0) == dwp.DWP_ERR_INVALID_VALUE
+    assert dwp.dwp_debug_warp_scan_trace(x.data_ptr(), 33, x.data_ptr(), 0) == dwp.DWP_ERR_INVALID_VALUE

@@ -84,3 +84,23 @@ def test_static_scratch_rejects_sizes_beyond_its_maximum():
     assert st == dwp.DWP_ERR_SCRATCH_TOO_SMALL
     assert lib.dwp_scan_static_scratch(dwp.DWP_U32_ADD, 7, None, None, 10, None) == dwp.DWP_ERR_INVALID_VALUE
     assert lib.dwp_scan_static_scratch(9, dwp.DWP_EXCLUSIVE, None, None, 10, None) == dwp.DWP_ERR_INVALID_VALUE
+
+
+def test_static_status_reports_a_device_timeout():
+    """The built-in array's status word is readable: a tile that never
+    publishes (fallback off, short spin) makes its successors record a
+    look-back timeout, which dwp_read_static_status returns; the next healthy
+    call clears it."""
+    st, b = dwp.dwp_scan_exclusive(dwp.DWP_U32_ADD, 0, 0, 1 << 30, 0, 0, 0)
+    tile = (1 << 30) // ((b - 128) // 8)
+    x = torch.from_numpy(synth.u32_small_values(2000 * tile, 44).view(np.int32)).cuda()
+    stream = torch.cuda.current_stream().cuda_stream
+    try:
+        dwp.dwp_debug_set_fault(5, 2000, 0xFFFFFFFF)
+        _static(x, "u32_add", False)
+        assert dwp.dwp_read_static_status(stream) == dwp.DWP_ERR_LOOKBACK_TIMEOUT
+    finally:
+        dwp.dwp_debug_set_fault(0xFFFFFFFF, 0, 0)
+    y = _static(x, "u32_add", False)
+    assert dwp.dwp_read_static_status(stream) == dwp.DWP_SUCCESS
+    assert torch.equal(y, _regular(x, "u32_add", False))
