@@ -153,6 +153,15 @@ class ClockSampler:
                 "window": "timed region" if inside else "last samples (timed region shorter than the sampling period)"}
 
 
+def host_cores() -> dict:
+    """Host CPU cores: all of them, and those this process may run on."""
+    try:
+        usable = len(os.sched_getaffinity(0))
+    except AttributeError:
+        usable = os.cpu_count()
+    return {"host_cores": os.cpu_count(), "usable_cores": usable}
+
+
 # ---------------------------------------------------------------- reference arm
 
 def run_reference(args, rank: int) -> None:
@@ -184,7 +193,7 @@ def run_reference(args, rank: int) -> None:
         "config": {"workload": "u32 exclusive sum scan, n=2^28, values uniform in [0, 2^32)",
                    "n": N_FULL, "sample_elements_per_step": per_step},
         "cpu_baseline": {"value": val, "unit": "Gelem/s", "cores": 1, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, **host_cores()},
         "e2e": {"value": val, "unit": "Gelem/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -200,7 +209,8 @@ def main() -> None:
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=10.0)
-    ap.add_argument("--only", default=None, choices=["segscan", "compact", "recurrence", "segreduce"],
+    ap.add_argument("--only", default=None,
+                    choices=["segscan", "compact", "recurrence", "segreduce", "compact_staged"],
                     help="time only this workload (at --log2n) and print its entry; for "
                          "profiler captures")
     ap.add_argument("--log2n", type=int, default=28,
@@ -272,34 +282,73 @@ def main() -> None:
     if dwp.read_status(scratch) != dwp.DWP_SUCCESS:
         raise RuntimeError("device status after warm-up: %s" % dwp.status_string(dwp.read_status(scratch)))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     barrier()
     wall0 = time.time()
     e0.record(stream)
-    for _ in range(args.steps):
+    for k in range(args.steps):
+        marks[k].record(stream)
         step()
+    marks[args.steps].record(stream)
     e1.record(stream)
     barrier()
     wall1 = time.time()
+    per_step = sorted(marks[k].elapsed_time(marks[k + 1]) for k in range(args.steps))
     st = dwp.read_status(scratch)
     if st != dwp.DWP_SUCCESS:
         raise RuntimeError("device status after timed steps: %s" % dwp.status_string(st))
     ms = max_over_ranks(e0.elapsed_time(e1) / args.steps)
     value = world * n / (ms * 1e-3) / 1e9
 
-    # end to end from pinned host memory through the same C entry point
+    # end to end from pinned host memory through the same C entry point:
+    # every step copies its input in, scans it and copies the result out.
+    # Serially on one stream, and pipelined over two streams with their own
+    # device buffers, so that one step's copy-out overlaps the next step's
+    # copy-in (the two directions use separate copy engines).
     e2e_steps = max(3, min(args.steps, 20))
-    y_host = torch.empty(n, dtype=torch.int32).pin_memory()
+    y_host = [torch.empty(n, dtype=torch.int32).pin_memory() for _ in range(2)]
     for _ in range(2):
-        x.copy_(x_host, non_blocking=True); step(); y_host.copy_(y, non_blocking=True)
+        x.copy_(x_host, non_blocking=True); step(); y_host[0].copy_(y, non_blocking=True)
     barrier()
     e0.record(stream)
     for _ in range(e2e_steps):
         x.copy_(x_host, non_blocking=True)
         step()
-        y_host.copy_(y, non_blocking=True)
+        y_host[0].copy_(y, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    e2e_serial_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps)
+    sides = [torch.cuda.Stream(dev) for _ in range(2)]
+    xs, ys, scr2 = [x, torch.empty_like(x)], [y, torch.empty_like(y)], [scratch, dwp.alloc_scratch(need, dev)]
+
+    def e2e_step(k):
+        j = k % 2
+        s = sides[j]
+        with torch.cuda.stream(s):
+            xs[j].copy_(x_host, non_blocking=True)
+            st = f(dwp.DWP_U32_ADD, ctypes.c_void_p(xs[j].data_ptr()), ctypes.c_void_p(ys[j].data_ptr()), n,
+                   ctypes.c_void_p(scr2[j].data_ptr()), ctypes.byref(sb), ctypes.c_void_p(int(s.cuda_stream)))
+            if st != 0:
+                raise RuntimeError(dwp.status_string(st))
+            y_host[j].copy_(ys[j], non_blocking=True)
+
+    for k in range(2):
+        e2e_step(k)
+    barrier()
+    e0.record(stream)
+    for s in sides:
+        s.wait_event(e0)
+    for k in range(e2e_steps):
+        e2e_step(k)
+    for s in sides:
+        stream.wait_stream(s)
     e1.record(stream)
     barrier()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps)
+    for j in range(2):
+        if dwp.read_status(scr2[j]) != dwp.DWP_SUCCESS:
+            raise RuntimeError("device status after the end-to-end steps")
+    del xs, ys, scr2
     if clocks is not None:
         clocks.stop()
 
@@ -316,7 +365,8 @@ def main() -> None:
             dist.destroy_process_group()
         return
 
-    cpu = cpu_baseline(x_host.numpy().view(np.uint32), args.cpu_budget_s)
+    # the oracle reads a pageable copy, as the reference arm does
+    cpu = cpu_baseline(x_host.numpy().view(np.uint32).copy(), args.cpu_budget_s)
     line = {
         "metric": METRIC,
         "value": value,
@@ -325,6 +375,8 @@ def main() -> None:
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": ms,
+        "ms_median": per_step[len(per_step) // 2],
+        "ms_min": per_step[0],
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -337,13 +389,15 @@ def main() -> None:
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                      "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)",
                      "algorithmic_bytes_per_launch": alg_bytes,
-                     "timing": "CUDA events over the whole C call (scratch clear + scan kernel)",
+                     "timing": "CUDA events over the whole C call (scratch-clear kernel + scan kernel)",
                      "traffic": profiled_traffic()},
         "cpu_baseline": cpu,
         "e2e": {"value": n / (e2e_ms * 1e-3) / 1e9, "unit": "Gelem/s",
                 "h2d_bytes_per_step": 4 * n, "d2h_bytes_per_step": 4 * n,
-                "ms_per_step": e2e_ms, "steps": e2e_steps},
-        "gpu_launches": args.steps,
+                "ms_per_step": e2e_ms, "steps": e2e_steps,
+                "how": "pinned host in and out, two steps in flight on two streams",
+                "serial_one_stream_ms_per_step": e2e_serial_ms},
+        "gpu_launches": 2 * args.steps,
         "clocks": clocks.summary(wall0, wall1) if clocks is not None else None,
         "secondary": secondary,
     }
@@ -365,21 +419,37 @@ def cpu_baseline(x: np.ndarray, budget_s: float) -> dict:
             break
     return {"value": runs * x.size / t_total / 1e9, "unit": "Gelem/s", "cores": 1, "kind": "oracle",
             "sample": "%d full passes over the n=2^%d input (%.1f s), sequential C oracle on one host core"
-                      % (runs, int(x.size).bit_length() - 1, t_total)}
+                      % (runs, int(x.size).bit_length() - 1, t_total), **host_cores()}
 
 
-def time_calls(fn, steps: int, warmup: int, stream) -> float:
+def time_calls(fn, steps: int, warmup: int, stream, stats: dict | None = None) -> float:
+    """Mean ms per call over `steps` back-to-back calls (one event pair
+    around all of them); with `stats`, also the median and minimum of the
+    per-call event pairs."""
     import torch
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(steps):
+    for k in range(steps):
         fn()
     e1.record(stream)
     torch.cuda.synchronize()
-    return e0.elapsed_time(e1) / steps
+    mean = e0.elapsed_time(e1) / steps
+    if stats is not None:
+        # a second pass with an event between calls; an event breaks the
+        # overlap of one call's launch with the previous call, so for short
+        # calls these figures run above the mean of the back-to-back pass
+        marks = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        for k in range(steps):
+            marks[k].record(stream)
+            fn()
+        marks[steps].record(stream)
+        torch.cuda.synchronize()
+        per = sorted(marks[k].elapsed_time(marks[k + 1]) for k in range(steps))
+        stats["ms_median"], stats["ms_min"] = per[len(per) // 2], per[0]
+    return mean
 
 
 def measure_secondary(dwp, lib, dev, stream, peaks, x, y, scratch, need) -> dict:
@@ -400,9 +470,10 @@ def measure_secondary(dwp, lib, dev, stream, peaks, x, y, scratch, need) -> dict
             src = xf
         args = (op, ctypes.c_void_p(src.data_ptr()), ctypes.c_void_p(y.data_ptr()), n,
                 ctypes.c_void_p(scratch.data_ptr()), ctypes.byref(sb), st_ptr)
-        ms = time_calls(lambda: entry(*args), 200, 5, stream)
+        stats = {}
+        ms = time_calls(lambda: entry(*args), 200, 5, stream, stats)
         gbs = 8 * n / (ms * 1e-3) / 1e9
-        out[name] = {"n": n, "ms": ms, "Gelem_s": n / (ms * 1e-3) / 1e9, "GB_s": gbs,
+        out[name] = {"n": n, "ms": ms, **stats, "Gelem_s": n / (ms * 1e-3) / 1e9, "GB_s": gbs,
                      "frac": gbs / peaks["hbm_gbs"]}
     del xf
     out["u32_add_exclusive_2p20"] = measure_small(dwp, lib, dev, stream)
@@ -411,6 +482,7 @@ def measure_secondary(dwp, lib, dev, stream, peaks, x, y, scratch, need) -> dict
     out["lookback_window_ablation"] = measure_window_ablation(dwp, lib, stream, x, y, scratch, need)
     out["segscan_u32_exclusive"] = measure_segscan(dwp, lib, dev, stream, peaks)
     out["compact_16B_records"] = measure_compact(dwp, lib, dev, stream, peaks)
+    out["compact_staged_vs_fused"] = measure_compact_staged(dwp, lib, dev, stream, peaks)
     out["linear_recurrence_f32"] = measure_recurrence(dwp, lib, dev, stream, peaks)
     out["segreduce_u32"] = measure_segreduce(dwp, lib, dev, stream, peaks)
     return out
@@ -430,13 +502,15 @@ def measure_small(dwp, lib, dev, stream, log2n=20, steps=2000, warmup=20) -> dic
     args = (dwp.DWP_U32_ADD, ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(y.data_ptr()), n,
             ctypes.c_void_p(scratch.data_ptr()), ctypes.byref(sb),
             ctypes.c_void_p(int(stream.cuda_stream)))
-    ms = time_calls(lambda: lib.dwp_scan_exclusive(*args), steps, warmup, stream)
-    return {"n": n, "us": ms * 1e3, "Gelem_s": n / (ms * 1e-3) / 1e9,
+    stats = {}
+    ms = time_calls(lambda: lib.dwp_scan_exclusive(*args), steps, warmup, stream, stats)
+    return {"n": n, "us": ms * 1e3, "us_median": stats["ms_median"] * 1e3, "us_min": stats["ms_min"] * 1e3,
+            "Gelem_s": n / (ms * 1e-3) / 1e9,
             "workload": "u32 exclusive sum scan, n=2^%d values in [0,16) (SplitMix64 seed 0xD3B00001), "
                         "L2-resident: launch-bound, not an HBM figure" % log2n}
 
 
-def measure_two_level(dwp, lib, dev, stream, log2ns=(12, 14, 16, 18, 20, 22, 24, 26), steps=500) -> dict:
+def measure_two_level(dwp, lib, dev, stream, log2ns=(12, 14, 16, 18, 19, 20, 21, 22, 23, 24, 26), steps=500) -> dict:
     """u32 exclusive add by the single-pass look-back scan and by the
     two-level three-launch form, microseconds per call, back to back."""
     import ctypes
@@ -523,7 +597,8 @@ def run_only(args) -> None:
     lib = dwp.load()
     stream = torch.cuda.current_stream(dev)
     fn = {"segscan": measure_segscan, "compact": measure_compact,
-          "recurrence": measure_recurrence, "segreduce": measure_segreduce}[args.only]
+          "recurrence": measure_recurrence, "segreduce": measure_segreduce,
+          "compact_staged": measure_compact_staged}[args.only]
     r = fn(dwp, lib, dev, stream, measured_peaks(), log2n=args.log2n, steps=args.steps,
            warmup=args.warmup)
     print(json.dumps({"only": args.only, **r}), flush=True)
@@ -546,16 +621,76 @@ def measure_compact(dwp, lib, dev, stream, peaks, log2n=26, steps=100, warmup=5)
             ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(cnt.data_ptr()),
             ctypes.c_void_p(scratch.data_ptr()), ctypes.byref(sb),
             ctypes.c_void_p(int(stream.cuda_stream)))
-    ms = time_calls(lambda: lib.dwp_compact_by_flags(*args), steps, warmup, stream)
+    stats = {}
+    ms = time_calls(lambda: lib.dwp_compact_by_flags(*args), steps, warmup, stream, stats)
     if dwp.read_status(scratch) != dwp.DWP_SUCCESS:
         raise RuntimeError("compaction reported a device-side error")
     k = int(cnt.item())
     alg = 17 * n + 16 * k + 4
     gbs = alg / (ms * 1e-3) / 1e9
-    return {"n": n, "kept": k, "ms": ms, "Gelem_s": n / (ms * 1e-3) / 1e9, "GB_s": gbs,
+    return {"n": n, "kept": k, "ms": ms, **stats, "Gelem_s": n / (ms * 1e-3) / 1e9, "GB_s": gbs,
             "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": alg,
             "workload": "stable compaction of 2^%d 16-byte records, keep flag Bernoulli(0.3) "
                         "(SplitMix64 seed 0xD3B00004)" % log2n}
+
+
+def kept_sector_bytes(flags: np.ndarray) -> int:
+    """Bytes of the 32-byte sectors that hold at least one kept 16-byte
+    record: what a compaction that reads only the kept records must read."""
+    f = flags != 0
+    if f.size % 2:
+        f = np.concatenate([f, [False]])
+    return int(f.reshape(-1, 2).any(axis=1).sum()) * 32
+
+
+def measure_compact_staged(dwp, lib, dev, stream, peaks, log2n=26, steps=50, warmup=5) -> dict:
+    """Staged compaction (u32 flags and their exclusive scan written to
+    memory, then a scatter: three launches and the scan's clear) against the
+    fused single-pass kernel, on the compaction workload, with the bytes each
+    moves.  Algorithmic bytes:
+      fused         n flags + 16n records read, 16k written, 4 count
+      staged        n flags read + 4n u32 flags written; the scan reads 4n and
+                    writes 4n; the scatter reads 4n flags, 4n offsets and the
+                    sectors holding kept records (S), writes 16k and the count
+      lower bound   n flags + S + 16k + 4: a compaction that reads only the
+                    sectors of kept records ("selective read")."""
+    import ctypes
+    import torch
+    n = 1 << log2n
+    rec = torch.from_numpy(synth.records(n).view(np.int32)).to(dev)
+    flags_np = synth.keep_flags(n)
+    flags = torch.from_numpy(flags_np).to(dev)
+    out = torch.empty_like(rec)
+    cnt = torch.zeros(1, dtype=torch.int32, device=dev)
+    res = {"n": n}
+    sector = kept_sector_bytes(flags_np)
+    for name, fn, need in (("fused", lib.dwp_compact_by_flags, dwp.compact_scratch_bytes(n)),
+                           ("staged", lib.dwp_compact_by_flags_staged, dwp.compact_staged_scratch_bytes(n))):
+        scratch = dwp.alloc_scratch(need, dev)
+        sb = ctypes.c_size_t(need)
+        args = (ctypes.c_void_p(rec.data_ptr()), ctypes.c_void_p(flags.data_ptr()), n,
+                ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(cnt.data_ptr()),
+                ctypes.c_void_p(scratch.data_ptr()), ctypes.byref(sb),
+                ctypes.c_void_p(int(stream.cuda_stream)))
+        stats = {}
+        ms = time_calls(lambda: fn(*args), steps, warmup, stream, stats)
+        if dwp.read_status(scratch) != dwp.DWP_SUCCESS:
+            raise RuntimeError("%s compaction reported a device-side error" % name)
+        k = int(cnt.item())
+        alg = 17 * n + 16 * k + 4 if name == "fused" else 21 * n + sector + 16 * k + 4
+        res[name] = {"ms": ms, **stats, "algorithmic_bytes": alg,
+                     "GB_s": alg / (ms * 1e-3) / 1e9, "frac": alg / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+        del scratch
+    k = int(cnt.item())
+    lower = n + sector + 16 * k + 4
+    res["kept"] = k
+    res["kept_sector_bytes"] = sector
+    res["selective_read_lower_bound"] = {
+        "bytes": lower, "ms_at_peak": lower / (peaks["hbm_gbs"] * 1e9) * 1e3,
+        "fused_frac_of_it": lower / (res["fused"]["ms"] * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+    res["staged_over_fused"] = res["staged"]["ms"] / res["fused"]["ms"]
+    res["extra_bytes_staged"] = res["staged"]["algorithmic_bytes"] - res["fused"]["algorithmic_bytes"]
+    return res
 
 
 def measure_segscan(dwp, lib, dev, stream, peaks, log2n=27, steps=200, warmup=5) -> dict:
@@ -575,12 +710,13 @@ def measure_segscan(dwp, lib, dev, stream, peaks, log2n=27, steps=200, warmup=5)
     args = (ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(off.data_ptr()), nseg,
             ctypes.c_void_p(y.data_ptr()), n, dwp.DWP_EXCLUSIVE, ctypes.c_void_p(scratch.data_ptr()),
             ctypes.byref(sb), ctypes.c_void_p(int(stream.cuda_stream)))
-    ms = time_calls(lambda: lib.dwp_segmented_scan_u32(*args), steps, warmup, stream)
+    stats = {}
+    ms = time_calls(lambda: lib.dwp_segmented_scan_u32(*args), steps, warmup, stream, stats)
     if dwp.read_status(scratch) != dwp.DWP_SUCCESS:
         raise RuntimeError("segmented scan reported a device-side error")
     alg = 8 * n + 4 * (nseg + 1)
     gbs = alg / (ms * 1e-3) / 1e9
-    return {"n": n, "segments": nseg, "ms": ms, "Gelem_s": n / (ms * 1e-3) / 1e9, "GB_s": gbs,
+    return {"n": n, "segments": nseg, "ms": ms, **stats, "Gelem_s": n / (ms * 1e-3) / 1e9, "GB_s": gbs,
             "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": alg,
             "workload": ("segmented exclusive u32 sum scan, n=2^%d values in [0,255], Zipf(1.2) " % log2n) +
                         "lengths capped at 2^22, 5% empty, CSR offsets (SplitMix64 seed 0xD3B00005)"}
@@ -603,12 +739,13 @@ def measure_segreduce(dwp, lib, dev, stream, peaks, log2n=27, steps=200, warmup=
     args = (ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(off.data_ptr()), nseg,
             ctypes.c_void_p(out.data_ptr()), n, ctypes.c_void_p(scratch.data_ptr()), ctypes.byref(sb),
             ctypes.c_void_p(int(stream.cuda_stream)))
-    ms = time_calls(lambda: lib.dwp_segmented_reduce_u32(*args), steps, warmup, stream)
+    stats = {}
+    ms = time_calls(lambda: lib.dwp_segmented_reduce_u32(*args), steps, warmup, stream, stats)
     if dwp.read_status(scratch) != dwp.DWP_SUCCESS:
         raise RuntimeError("segmented reduction reported a device-side error")
     alg = 4 * n + 4 * (nseg + 1) + 4 * nseg
     gbs = alg / (ms * 1e-3) / 1e9
-    return {"n": n, "segments": nseg, "ms": ms, "Gelem_s": n / (ms * 1e-3) / 1e9, "GB_s": gbs,
+    return {"n": n, "segments": nseg, "ms": ms, **stats, "Gelem_s": n / (ms * 1e-3) / 1e9, "GB_s": gbs,
             "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": alg,
             "workload": ("segmented u32 sum reduction, n=2^%d values in [0,255], Zipf(1.2) " % log2n) +
                         "lengths capped at 2^22, 5% empty, CSR offsets (SplitMix64 seed 0xD3B00005)"}
@@ -629,12 +766,13 @@ def measure_recurrence(dwp, lib, dev, stream, peaks, log2n=28, steps=200, warmup
     args = (ctypes.c_void_p(a.data_ptr()), ctypes.c_void_p(b.data_ptr()), ctypes.c_void_p(h.data_ptr()),
             n, dwp.DWP_INCLUSIVE, ctypes.c_void_p(scratch.data_ptr()), ctypes.byref(sb),
             ctypes.c_void_p(int(stream.cuda_stream)))
-    ms = time_calls(lambda: lib.dwp_linear_recurrence_f32(*args), steps, warmup, stream)
+    stats = {}
+    ms = time_calls(lambda: lib.dwp_linear_recurrence_f32(*args), steps, warmup, stream, stats)
     if dwp.read_status(scratch) != dwp.DWP_SUCCESS:
         raise RuntimeError("linear recurrence reported a device-side error")
     alg = 12 * n
     gbs = alg / (ms * 1e-3) / 1e9
-    return {"n": n, "ms": ms, "Gelem_s": n / (ms * 1e-3) / 1e9, "GB_s": gbs,
+    return {"n": n, "ms": ms, **stats, "Gelem_s": n / (ms * 1e-3) / 1e9, "GB_s": gbs,
             "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": alg,
             "workload": "f32 linear recurrence h[t] = a[t] h[t-1] + b[t], inclusive, n=2^%d, "
                         "a uniform in [0.5,1), b uniform in [-1,1) (SplitMix64 seeds 0xD3B00006/7)"

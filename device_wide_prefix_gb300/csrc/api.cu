@@ -1,6 +1,9 @@
 // C entry points: argument validation, the scratch size query, the scratch
 // clear and the launch.  Validation happens before any CUDA call, so an
-// argument error never enqueues work.
+// argument error never enqueues work.  The scratch is cleared by a small
+// kernel of the library rather than cudaMemsetAsync, so that the kernel
+// after it can be launched programmatically (launch_pdl) and overlap its
+// launch with the clear.
 #include <cuda_runtime.h>
 
 #include <cstddef>
@@ -31,8 +34,7 @@ dwp_status scan_common(bool inclusive, dwp_op op, const void *in, void *out, siz
     const int iop = static_cast<int>(op);
     if (iop != DWP_U32_ADD && iop != DWP_F32_ADD && iop != DWP_U32_MAX) return DWP_ERR_INVALID_VALUE;
     if (uint64_t(n) > kMaxN) return DWP_ERR_INVALID_VALUE;
-    const uint64_t tiles = ceil_div(n, scan_tile_elems());
-    const size_t need = scratch_bytes_for_tiles(tiles);
+    const size_t need = scratch_bytes_for_tiles(scan_tiles(n));
     if (!scratch) {
         *scratch_bytes = need;
         return DWP_SUCCESS;
@@ -47,7 +49,7 @@ dwp_status scan_common(bool inclusive, dwp_op op, const void *in, void *out, siz
         return DWP_ERR_ALIASING;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(scratch, 0, need, s) != cudaSuccess) {
+    if (launch_clear(scratch, need, nullptr, 0, s) != cudaSuccess) {
         cudaGetLastError();
         return DWP_ERR_CUDA;
     }
@@ -82,7 +84,7 @@ dwp_status two_level_common(dwp_op op, dwp_mode mode, const void *in, void *out,
         return DWP_ERR_ALIASING;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     // only the status word needs clearing: the totals are written before use
-    if (cudaMemsetAsync(scratch, 0, kHeaderBytes, s) != cudaSuccess) {
+    if (launch_clear(scratch, kHeaderBytes, nullptr, 0, s) != cudaSuccess) {
         cudaGetLastError();
         return DWP_ERR_CUDA;
     }
@@ -122,7 +124,7 @@ dwp_status segscan_common(const uint32_t *values, const uint32_t *offsets, size_
         return DWP_ERR_ALIASING;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(scratch, 0, need, s) != cudaSuccess) {
+    if (launch_clear(scratch, need, nullptr, 0, s) != cudaSuccess) {
         cudaGetLastError();
         return DWP_ERR_CUDA;
     }
@@ -160,17 +162,12 @@ dwp_status compact_common(const void *records, const uint8_t *flags, size_t n, v
         return DWP_ERR_ALIASING;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(scratch, 0, need, s) != cudaSuccess) {
+    // n == 0: the count is cleared with the scratch, and nothing else runs
+    if (launch_clear(scratch, need, n == 0 ? count : nullptr, sizeof(uint32_t), s) != cudaSuccess) {
         cudaGetLastError();
         return DWP_ERR_CUDA;
     }
-    if (n == 0) {
-        if (cudaMemsetAsync(count, 0, sizeof(uint32_t), s) != cudaSuccess) {
-            cudaGetLastError();
-            return DWP_ERR_CUDA;
-        }
-        return DWP_SUCCESS;
-    }
+    if (n == 0) return DWP_SUCCESS;
     if (launch_compact(records, flags, n, out, count, scratch, s) != cudaSuccess) {
         cudaGetLastError();
         return DWP_ERR_CUDA;
@@ -202,8 +199,7 @@ dwp_status segreduce_common(const uint32_t *values, const uint32_t *offsets, siz
         return DWP_ERR_ALIASING;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(scratch, 0, need, s) != cudaSuccess ||
-        (nseg > 0 && cudaMemsetAsync(out, 0, rbytes, s) != cudaSuccess)) {
+    if (launch_clear(scratch, need, nseg > 0 ? out : nullptr, rbytes, s) != cudaSuccess) {
         cudaGetLastError();
         return DWP_ERR_CUDA;
     }
@@ -240,7 +236,7 @@ dwp_status recurrence_common(const float *a, const float *b, float *h, size_t n,
         return DWP_ERR_ALIASING;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(scratch, 0, need, s) != cudaSuccess) {
+    if (launch_clear(scratch, need, nullptr, 0, s) != cudaSuccess) {
         cudaGetLastError();
         return DWP_ERR_CUDA;
     }

@@ -189,6 +189,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         fence_mbar_init();
     }
     __syncthreads();
+    // shared memory only so far; the kernel before may still be running.
+    // No early trigger: the next kernel launches as the blocks exit (an
+    // early one measured slower for this persistent kernel)
+    pdl_wait();
 
     // valid records of tile t, and how many of its flag bytes the bulk copy
     // brings (a multiple of 16; the rest are read from global memory)
@@ -451,10 +455,9 @@ cudaError_t launch_compact(const void *records, const uint8_t *flags, uint64_t n
     const uint32_t grid = uint32_t(tiles < uint64_t(dev_blocks) ? tiles : uint64_t(dev_blocks));
     auto *hdr = reinterpret_cast<ScratchHeader *>(scratch);
     auto *desc = reinterpret_cast<uint64_t *>(static_cast<unsigned char *>(scratch) + kHeaderBytes);
-    kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(
-        reinterpret_cast<const uint4 *>(records), flags, n, reinterpret_cast<uint4 *>(out), count,
-        uint32_t(tiles), hdr, desc, fault);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(C::kThreads), C::kSmemBytes, stream,
+                      reinterpret_cast<const uint4 *>(records), flags, n,
+                      reinterpret_cast<uint4 *>(out), count, uint32_t(tiles), hdr, desc, fault);
 }
 
 }  // namespace dwp

@@ -31,6 +31,8 @@ constexpr int kStagedThreads = 256;
 // four 16-byte stores), the last n % 16 flags one by one.
 __global__ void __launch_bounds__(kStagedThreads)
     predicate_kernel(const uint8_t *flags, uint32_t *f, uint64_t n) {
+    pdl_wait();
+    pdl_trigger();
     const uint64_t nvec = n / 16;
     const uint64_t stride = uint64_t(gridDim.x) * blockDim.x;
     for (uint64_t q = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x; q < nvec; q += stride) {
@@ -54,6 +56,8 @@ __global__ void __launch_bounds__(kStagedThreads)
 __global__ void __launch_bounds__(kStagedThreads)
     scatter_kernel(const uint4 *rec, const uint32_t *f, const uint32_t *off, uint64_t n, uint4 *out,
                    uint32_t *count) {
+    pdl_wait();
+    pdl_trigger();
     const uint64_t nvec = n / 4;
     const uint64_t stride = uint64_t(gridDim.x) * blockDim.x;
     for (uint64_t q = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x; q < nvec; q += stride) {
@@ -135,7 +139,7 @@ extern "C" dwp_status dwp_compact_by_flags_staged(const void *d_records, const u
         size_t sb = scan_need;
         st = dwp_scan_exclusive(DWP_U32_ADD, nullptr, nullptr, 0, d_scratch, &sb, stream);
         if (st != DWP_SUCCESS) return st;
-        if (cudaMemsetAsync(d_count, 0, sizeof(uint32_t), s) != cudaSuccess) {
+        if (launch_clear(d_count, sizeof(uint32_t), nullptr, 0, s) != cudaSuccess) {
             cudaGetLastError();
             return DWP_ERR_CUDA;
         }
@@ -144,13 +148,20 @@ extern "C" dwp_status dwp_compact_by_flags_staged(const void *d_records, const u
     const uint32_t g1 = staged_grid(reinterpret_cast<const void *>(predicate_kernel), (n + 15) / 16);
     const uint32_t g3 = staged_grid(reinterpret_cast<const void *>(scatter_kernel), (n + 3) / 4);
     if (g1 == 0 || g3 == 0) return DWP_ERR_CUDA;
-    predicate_kernel<<<g1, kStagedThreads, 0, s>>>(d_flags, f, n);
-    if (cudaGetLastError() != cudaSuccess) return DWP_ERR_CUDA;
+    if (launch_pdl(predicate_kernel, dim3(g1), dim3(kStagedThreads), 0, s, d_flags, f, uint64_t(n)) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return DWP_ERR_CUDA;
+    }
     size_t sb = scan_need;
     st = dwp_scan_exclusive(DWP_U32_ADD, f, off, n, d_scratch, &sb, stream);
     if (st != DWP_SUCCESS) return st;
-    scatter_kernel<<<g3, kStagedThreads, 0, s>>>(static_cast<const uint4 *>(d_records), f, off, n,
-                                                 static_cast<uint4 *>(d_out), d_count);
-    if (cudaGetLastError() != cudaSuccess) return DWP_ERR_CUDA;
+    if (launch_pdl(scatter_kernel, dim3(g3), dim3(kStagedThreads), 0, s,
+                   static_cast<const uint4 *>(d_records), static_cast<const uint32_t *>(f),
+                   static_cast<const uint32_t *>(off), uint64_t(n), static_cast<uint4 *>(d_out),
+                   d_count) != cudaSuccess) {
+        cudaGetLastError();
+        return DWP_ERR_CUDA;
+    }
     return DWP_SUCCESS;
 }

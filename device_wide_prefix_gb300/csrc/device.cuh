@@ -72,6 +72,21 @@ struct OpF32Add {
 // ---------------------------------------------------------------------------
 // Small PTX wrappers.
 
+// Programmatic dependent launch.  Every kernel of the library is launched
+// with programmatic stream serialisation, so it may start while the kernel
+// before it on the stream is still running.  pdl_wait() blocks until that
+// kernel (and, through its own wait, everything before it) has completed
+// and its memory is visible; every kernel calls it before its first access
+// to global memory.  pdl_trigger() lets the next kernel on the stream start
+// its launch early; that kernel waits the same way before touching memory.
+// The scratch-clear kernel and the short kernels trigger at once; the
+// persistent look-back kernels do not (their blocks trigger as they exit),
+// which measured faster on GB300 at every size.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -491,5 +506,34 @@ __device__ __forceinline__ int lookback(uint64_t *desc, uint32_t t, uint32_t lan
     *carry_out = carry;
     return 0;
 }
+
+// ---------------------------------------------------------------------------
+// Decoupled Fallback for the plain scan: the descriptor tile p would
+// publish, reduced by one warp straight from the input (tile 0's aggregate
+// is its inclusive prefix).
+template <class Op, int TILE>
+struct ScanRescue {
+    static_assert(TILE % 4 == 0, "full tiles are read as 16-byte vectors");
+    const typename Op::T *in;
+    uint64_t n;
+    __device__ uint64_t operator()(uint32_t p, uint32_t lane, uint32_t *scratch) const {
+        using T = typename Op::T;
+        const uint64_t b = uint64_t(p) * TILE;
+        const uint64_t e = min(n, b + uint64_t(TILE));
+        T acc = Op::identity();
+        if (e - b == uint64_t(TILE)) {
+            const uint4 *v4 = reinterpret_cast<const uint4 *>(in + b);
+            for (uint32_t q = lane; q < uint32_t(TILE) / 4u; q += 32u) {
+                const uint4 v = v4[q];
+                acc = Op::combine(acc, Op::combine(Op::combine(Op::from_bits(v.x), Op::from_bits(v.y)),
+                                                   Op::combine(Op::from_bits(v.z), Op::from_bits(v.w))));
+            }
+        } else {
+            for (uint64_t q = b + lane; q < e; q += 32u) acc = Op::combine(acc, in[q]);
+        }
+        const T tot = Op::warp_reduce(acc, lane, scratch);
+        return make_desc(p == 0 ? kPrefix : kAggregate, Op::to_bits(tot));
+    }
+};
 
 }  // namespace dwp

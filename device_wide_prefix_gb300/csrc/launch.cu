@@ -6,9 +6,54 @@
 #include <mutex>
 #include <utility>
 
+#include "device.cuh"
 #include "launch.h"
 
 namespace dwp {
+
+namespace {
+
+struct ClearRange {
+    uint32_t *p;
+    uint64_t words;
+};
+
+// Words up to the first 16-byte boundary one by one, then 16-byte stores,
+// then the last 0-3 words; grid-stride over the 16-byte part.
+__device__ __forceinline__ void clear_range(const ClearRange &r, uint64_t tid, uint64_t nthr) {
+    if (r.words == 0) return;
+    const uint64_t mis = (reinterpret_cast<uintptr_t>(r.p) >> 2) & 3u;
+    const uint64_t head = min(r.words, (4u - mis) & 3u);
+    const uint64_t vec = (r.words - head) / 4u;
+    const uint64_t tail0 = head + 4u * vec;
+    if (tid < head) r.p[tid] = 0u;
+    uint4 *v = reinterpret_cast<uint4 *>(r.p + head);
+    for (uint64_t i = tid; i < vec; i += nthr) v[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (tid < r.words - tail0) r.p[tail0 + tid] = 0u;
+}
+
+constexpr int kClearThreads = 256;
+
+__global__ void __launch_bounds__(kClearThreads) clear_kernel(ClearRange r0, ClearRange r1) {
+    pdl_trigger();
+    pdl_wait();  // the previous kernel may still use these bytes
+    const uint64_t tid = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    const uint64_t nthr = uint64_t(gridDim.x) * blockDim.x;
+    clear_range(r0, tid, nthr);
+    clear_range(r1, tid, nthr);
+}
+
+}  // namespace
+
+cudaError_t launch_clear(void *a, size_t a_bytes, void *b, size_t b_bytes, cudaStream_t stream) {
+    const ClearRange r0{static_cast<uint32_t *>(a), a ? uint64_t(a_bytes) / 4u : 0u};
+    const ClearRange r1{static_cast<uint32_t *>(b), b ? uint64_t(b_bytes) / 4u : 0u};
+    if (r0.words == 0 && r1.words == 0) return cudaSuccess;
+    const uint64_t vec = (r0.words > r1.words ? r0.words : r1.words) / 4u + 1u;
+    uint64_t blocks = (vec + kClearThreads - 1) / kClearThreads;
+    if (blocks > 1024u) blocks = 1024u;
+    return launch_pdl(clear_kernel, dim3(uint32_t(blocks)), dim3(kClearThreads), 0, stream, r0, r1);
+}
 
 namespace {
 std::mutex g_mu;

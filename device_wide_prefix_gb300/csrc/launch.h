@@ -7,17 +7,57 @@
 
 namespace dwp {
 
+// Launch `kernel` with programmatic stream serialisation: it may begin while
+// the previous kernel on `stream` finishes, and waits for it (pdl_wait)
+// before it touches global memory.  Hides most of one launch latency per
+// kernel boundary.
+template <class... KArgs, class... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// Zero [a, a + a_bytes) and [b, b + b_bytes) with one kernel on `stream`
+// (launched like every other kernel here, so the kernel after it can start
+// early).  Both pointers 4-byte aligned and both sizes multiples of 4 bytes;
+// a null pointer or a zero size skips that range.
+cudaError_t launch_clear(void *a, size_t a_bytes, void *b, size_t b_bytes, cudaStream_t stream);
+
 // Resident blocks of `kernel` on the current device (SM count x blocks per
 // SM at this block size and dynamic shared memory).  Also raises the
 // kernel's dynamic shared-memory limit to `smem_bytes`.  Cached per device
 // and kernel.  Returns 0 if the kernel cannot be resident at all.
 int device_blocks(const void *kernel, int threads, size_t smem_bytes);
 
-// Elements per tile of the plain scan kernel.
+// Inputs of at most this many elements take the small-input plain scan
+// (scan_small.cu: one block per tile, registers only); larger ones the
+// persistent pipelined kernel (scan.cu).
+constexpr uint64_t kScanSmallMax = uint64_t(1) << 22;
+// Elements per tile of the two plain scan kernels (the small-input one
+// sizes its tile by n).
 uint32_t scan_tile_elems();
-// One launch of the plain scan (the scratch has already been cleared).
+uint32_t scan_small_tile_elems(uint64_t n);
+// Tiles, so descriptors, the plain scan uses for n elements.
+inline uint64_t scan_tiles(uint64_t n) {
+    const uint64_t tile = n <= kScanSmallMax ? scan_small_tile_elems(n) : scan_tile_elems();
+    return (n + tile - 1) / tile;
+}
+// One launch of the plain scan (the scratch has already been cleared); picks
+// the kernel by n as above.
 cudaError_t launch_scan(dwp_op op, bool inclusive, const void *in, void *out, uint64_t n,
                         void *scratch, cudaStream_t stream);
+cudaError_t launch_scan_small(dwp_op op, bool inclusive, const void *in, void *out, uint64_t n,
+                              void *scratch, cudaStream_t stream, const LaunchKnobs &fault);
 
 // Elements per tile of the segmented scan kernel.
 uint32_t segscan_tile_elems();

@@ -320,7 +320,11 @@ __device__ __forceinline__ int lookback_affine(uint64_t *desc, uint32_t t, uint3
     return 0;
 }
 
-template <bool INCL, class C>
+// PERTURB compiles in the schedule-perturbation points of the test hook
+// dwp_debug_set_delay.  Launches pick the variant without them unless the
+// hook is on: in this kernel the inlined points alone (never taken) cost
+// measurable time, so production launches carry none of their code.
+template <bool INCL, class C, bool PERTURB>
 __global__ void __launch_bounds__(C::kThreads, 1)
     recurrence_kernel(const float *ga, const float *gb, float *out, uint64_t n, uint32_t num_tiles,
                       ScratchHeader *hdr, uint64_t *desc, LaunchKnobs fault) {
@@ -353,6 +357,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         fence_mbar_init();
     }
     __syncthreads();
+    // shared memory only so far; the kernel before may still be running.
+    // No early trigger: the next kernel launches as the blocks exit (an
+    // early one measured slower for this persistent kernel)
+    pdl_wait();
 
     auto tile_extent = [&](uint32_t t, uint32_t &valid, uint32_t &bulk) {
         const uint64_t rem = n - uint64_t(t) * TILE;
@@ -382,7 +390,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 if (ld_volatile_smem(sm.abort_flag()) == 0) {
                     t = atomicAdd(&hdr->tile_counter, 1u);
                     if (t >= num_tiles) t = kNoTile;
-                    else perturb(fault, t, kSiteDraw);
+                    else if (PERTURB) perturb(fault, t, kSiteDraw);
                 }
                 *reinterpret_cast<volatile uint32_t *>(sm.tile_id(gi)) = t;
                 ++taken;
@@ -465,10 +473,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 const uint32_t c = lane + 32u * w2;
                 float A = 1.0f, B = 0.0f;
                 // vectors wherever the thread's items are all bulk-copied (a
-                // ragged last tile too), element by element only for the
-                // thread holding the 1-3 elements after the bulk part; a
-                // thread past the end keeps the identity map
-                if (c * ITEMS + ITEMS <= bulk) {
+                // ragged last tile too; the test on `valid` first keeps the
+                // usual full tile on one warp-uniform path), element by
+                // element only for the thread holding the 1-3 elements after
+                // the bulk part; a thread past the end keeps the identity map
+                if (valid == uint32_t(TILE) || c * ITEMS + ITEMS <= bulk) {
                     const float4 *a4 = reinterpret_cast<const float4 *>(sa) + c * (ITEMS / 4);
                     const float4 *b4 = reinterpret_cast<const float4 *>(sb) + c * (ITEMS / 4);
 #pragma unroll
@@ -532,14 +541,14 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 pa[prefix_slot(lane * PER + j)] = __fmul_rn(mA[j], eA);
                 pb[prefix_slot(lane * PER + j)] = __fmaf_rn(mA[j], eB, mB[j]);
             }
-            perturb(fault, t, kSiteAggregate);
+            if (PERTURB) perturb(fault, t, kSiteAggregate);
             if (lane == 0) {
                 if (t != fault.never_publish_tile) {
                     if (t == 0) {
                         st_relaxed_gpu(desc + 1, make_desc(kPrefix, __float_as_uint(gB)));
                     } else {
                         st_relaxed_gpu(desc + 2 * uint64_t(t), make_desc(kAggregate, __float_as_uint(gA)));
-                        perturb(fault, t, kSiteMidWord);
+                        if (PERTURB) perturb(fault, t, kSiteMidWord);
                         st_relaxed_gpu(desc + 2 * uint64_t(t) + 1,
                                        make_desc(kAggregate, __float_as_uint(gB)));
                     }
@@ -574,11 +583,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             if (!draining && ld_volatile_smem(sm.abort_flag()) != 0) draining = true;
             float carry = 0.0f;
             int rc = (draining || ld_volatile_smem(sm.lbres(i)) != 0u) ? 1 : 0;
-            if (rc == 0) perturb(fault, t, kSiteLookback);
+            if (PERTURB && rc == 0) perturb(fault, t, kSiteLookback);
             if (rc == 0 && t != 0)
                 rc = lookback_affine(desc, t, lane, fault.spin_limit, fault.fallback_polls, rescue,
                                      &hdr->fallbacks, scr, &carry);
-            if (rc == 0) perturb(fault, t, kSitePrefix);
+            if (PERTURB && rc == 0) perturb(fault, t, kSitePrefix);
             if (lane == 0) {
                 if (rc == 0) {
                     if (t != 0 && t != fault.never_publish_tile)
@@ -672,7 +681,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         float h = __fmaf_rn(sm.pre_a(i)[prefix_slot(c)], *sm.carry(i), sm.pre_b(i)[prefix_slot(c)]);
         __syncwarp();
         if (lane == 0) mbar_arrive(sm.info_free(i));
-        if (p0 + ITEMS <= bulk) {
+        if (valid == uint32_t(TILE) || p0 + ITEMS <= bulk) {
             const float4 *a4 = reinterpret_cast<const float4 *>(sa + p0);
             float4 *b4 = reinterpret_cast<float4 *>(sb + p0);
 #pragma unroll
@@ -738,7 +747,7 @@ template <bool INCL>
 cudaError_t launch_rec(const float *a, const float *b, float *h, uint64_t n, void *scratch,
                        cudaStream_t stream, const LaunchKnobs &fault) {
     using C = RecCfg;
-    auto kern = recurrence_kernel<INCL, C>;
+    auto kern = fault.delay_threshold != 0u ? recurrence_kernel<INCL, C, true> : recurrence_kernel<INCL, C, false>;
     const int dev_blocks = device_blocks(reinterpret_cast<const void *>(kern), C::kThreads,
                                          C::kSmemBytes);
     if (dev_blocks <= 0) return cudaErrorInvalidConfiguration;
@@ -746,8 +755,8 @@ cudaError_t launch_rec(const float *a, const float *b, float *h, uint64_t n, voi
     const uint32_t grid = uint32_t(tiles < uint64_t(dev_blocks) ? tiles : uint64_t(dev_blocks));
     auto *hdr = reinterpret_cast<ScratchHeader *>(scratch);
     auto *desc = reinterpret_cast<uint64_t *>(static_cast<unsigned char *>(scratch) + kHeaderBytes);
-    kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(a, b, h, n, uint32_t(tiles), hdr, desc, fault);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(C::kThreads), C::kSmemBytes, stream, a, b, h, n,
+                      uint32_t(tiles), hdr, desc, fault);
 }
 
 }  // namespace

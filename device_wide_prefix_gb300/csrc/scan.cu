@@ -161,45 +161,19 @@ struct ScanSmem {
     __device__ uint32_t *lb_scratch(int j) const { return abort_flag() + 4 + 33 * (C::kIn + j); }
 };
 
-// Element pos of a tile: from the stage buffer below `bulk`, from global
-// memory below `valid` (the ragged tail the bulk copy cannot cover), else the
-// identity.
+// Elements pos .. pos+3 of a tile as one vector when they lie past the
+// bulk-copied part: from global memory below `valid`, the identity (bit
+// pattern 0 for every operator here) past it.  Only the 1-3 elements after
+// a ragged tile's bulk part come this way.
 template <class Op>
-__device__ __forceinline__ typename Op::T tile_elem(const uint32_t *buf, const typename Op::T *in,
-                                                    uint64_t base, uint32_t pos, uint32_t bulk,
-                                                    uint32_t valid) {
-    if (pos < bulk) return Op::from_bits(buf[pos]);
-    if (pos < valid) return in[base + pos];
-    return Op::identity();
+__device__ __forceinline__ uint4 tail_vec(const typename Op::T *in, uint64_t base, uint32_t pos,
+                                          uint32_t valid) {
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+        w[e] = pos + e < valid ? Op::to_bits(in[base + pos + e]) : Op::to_bits(Op::identity());
+    return make_uint4(w[0], w[1], w[2], w[3]);
 }
-
-// Decoupled Fallback for the plain scan: the descriptor tile p would
-// publish, reduced by one warp straight from the input (tile 0's aggregate
-// is its inclusive prefix).
-template <class Op, int TILE>
-struct ScanRescue {
-    static_assert(TILE % 4 == 0, "full tiles are read as 16-byte vectors");
-    const typename Op::T *in;
-    uint64_t n;
-    __device__ uint64_t operator()(uint32_t p, uint32_t lane, uint32_t *scratch) const {
-        using T = typename Op::T;
-        const uint64_t b = uint64_t(p) * TILE;
-        const uint64_t e = min(n, b + uint64_t(TILE));
-        T acc = Op::identity();
-        if (e - b == uint64_t(TILE)) {
-            const uint4 *v4 = reinterpret_cast<const uint4 *>(in + b);
-            for (uint32_t q = lane; q < uint32_t(TILE) / 4u; q += 32u) {
-                const uint4 v = v4[q];
-                acc = Op::combine(acc, Op::combine(Op::combine(Op::from_bits(v.x), Op::from_bits(v.y)),
-                                                   Op::combine(Op::from_bits(v.z), Op::from_bits(v.w))));
-            }
-        } else {
-            for (uint64_t q = b + lane; q < e; q += 32u) acc = Op::combine(acc, in[q]);
-        }
-        const T tot = Op::warp_reduce(acc, lane, scratch);
-        return make_desc(p == 0 ? kPrefix : kAggregate, Op::to_bits(tot));
-    }
-};
 
 template <class Op, bool INCL, class C>
 __global__ void __launch_bounds__(C::kThreads, 1)
@@ -236,6 +210,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         fence_mbar_init();
     }
     __syncthreads();
+    // shared memory only so far; the kernel before may still be running.
+    // No early trigger: the next kernel launches as the blocks exit (an
+    // early one measured slower for this persistent kernel)
+    pdl_wait();
 
     auto tile_extent = [&](uint32_t t, uint32_t &valid, uint32_t &bulk) {
         const uint64_t rem = n - uint64_t(t) * TILE;
@@ -350,30 +328,43 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             uint32_t *pre = sm.prefix(i);
             uint32_t *lt = sm.lane_tot(s);
             // totals of consumer threads c = lane + 32*w, whose ITEMS
-            // contiguous elements start at c*ITEMS.  A thread whose items
-            // all lie in the bulk-copied part reads them as 16-byte vectors
-            // (in a ragged last tile too); only the one thread that holds
-            // the last 1-3 elements past the bulk part reads element by
-            // element, and threads wholly past the end contribute nothing.
+            // contiguous elements start at c*ITEMS, read as 16-byte vectors
+            // from the stage (the bulk part is a multiple of 4 elements, so
+            // a vector lies wholly inside it or wholly past it).  In a
+            // ragged last tile the 1-3 elements past the bulk part come from
+            // global memory, and threads wholly past the end add nothing.
             T tot[NW];
             const uint4 *v4 = reinterpret_cast<const uint4 *>(buf);
+            if (valid == uint32_t(TILE)) {  // every tile but a ragged last one
 #pragma unroll
-            for (int w2 = 0; w2 < NW; ++w2) {
-                const uint32_t c = lane + 32u * w2;
-                const uint32_t p0 = c * ITEMS;
-                T acc = Op::identity();
-                if (p0 + ITEMS <= bulk) {
+                for (int w2 = 0; w2 < NW; ++w2) {
+                    const uint32_t c = lane + 32u * w2;
+                    T acc = Op::identity();
 #pragma unroll
                     for (int v = 0; v < ITEMS / 4; ++v) {
                         const uint4 q = v4[c * (ITEMS / 4) + v];
                         acc = Op::combine(acc, Op::combine(Op::combine(Op::from_bits(q.x), Op::from_bits(q.y)),
                                                            Op::combine(Op::from_bits(q.z), Op::from_bits(q.w))));
                     }
-                } else if (p0 < valid) {
-                    for (int j = 0; j < ITEMS; ++j)
-                        acc = Op::combine(acc, tile_elem<Op>(buf, in, base, p0 + j, bulk, valid));
+                    tot[w2] = acc;
+                }
+            } else {
+#pragma unroll
+            for (int w2 = 0; w2 < NW; ++w2) {
+                const uint32_t c = lane + 32u * w2;
+                const uint32_t p0 = c * ITEMS;
+                T acc = Op::identity();
+                if (p0 < valid) {
+#pragma unroll
+                    for (int v = 0; v < ITEMS / 4; ++v) {
+                        const uint32_t pos = p0 + 4u * v;
+                        const uint4 q = pos < bulk ? v4[c * (ITEMS / 4) + v] : tail_vec<Op>(in, base, pos, valid);
+                        acc = Op::combine(acc, Op::combine(Op::combine(Op::from_bits(q.x), Op::from_bits(q.y)),
+                                                           Op::combine(Op::from_bits(q.z), Op::from_bits(q.w))));
+                    }
                 }
                 tot[w2] = acc;
+            }
             }
             // the input stage is no longer needed
             __syncwarp();
@@ -538,10 +529,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         T acc = Op::combine(Op::from_bits(*sm.carry(i)), Op::from_bits(sm.prefix(i)[prefix_slot(c)]));
         __syncwarp();
         if (lane == 0) mbar_arrive(sm.info_free(i));  // the info slot has been read
-        // as in the reduce: vectors wherever the thread's items are all in
-        // the bulk part, element by element only for the thread holding the
-        // ragged 1-3 elements after it, nothing past the end
-        if (p0 + ITEMS <= bulk) {
+        if (valid == uint32_t(TILE)) {  // every tile but a ragged last one
             uint4 *v4 = reinterpret_cast<uint4 *>(buf + p0);
 #pragma unroll
             for (int v = 0; v < ITEMS / 4; ++v) {
@@ -562,21 +550,35 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 v4[v] = make_uint4(r[0], r[1], r[2], r[3]);
             }
         } else if (p0 < valid) {
-            for (int j = 0; j < ITEMS; ++j) {
-                const uint32_t pos = p0 + j;
-                const T xv = tile_elem<Op>(buf, in, base, pos, bulk, valid);
-                T yv;
-                if (INCL) {
-                    acc = Op::combine(acc, xv);
-                    yv = acc;
-                } else {
-                    yv = acc;
-                    acc = Op::combine(acc, xv);
+            // as in the reduce: 16-byte vectors in the stage, written back
+            // in place; the 1-3 elements past the bulk part are read from
+            // and written to global memory; nothing past the end
+            uint4 *v4 = reinterpret_cast<uint4 *>(buf + p0);
+#pragma unroll
+            for (int v = 0; v < ITEMS / 4; ++v) {
+                const uint32_t pos = p0 + 4u * v;
+                const bool staged = pos < bulk;
+                const uint4 q = staged ? v4[v] : tail_vec<Op>(in, base, pos, valid);
+                const uint32_t qq[4] = {q.x, q.y, q.z, q.w};
+                uint32_t r[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const T xv = Op::from_bits(qq[e]);
+                    if (INCL) {
+                        acc = Op::combine(acc, xv);
+                        r[e] = Op::to_bits(acc);
+                    } else {
+                        r[e] = Op::to_bits(acc);
+                        acc = Op::combine(acc, xv);
+                    }
                 }
-                if (pos < bulk)
-                    buf[pos] = Op::to_bits(yv);
-                else if (pos < valid)
-                    out[base + pos] = yv;
+                if (staged) {
+                    v4[v] = make_uint4(r[0], r[1], r[2], r[3]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (pos + e < valid) out[base + pos + e] = Op::from_bits(r[e]);
+                }
             }
         }
         fence_proxy_async_smem();
@@ -618,10 +620,9 @@ cudaError_t launch_one(const void *in, void *out, uint64_t n, void *scratch, cud
     const uint32_t grid = uint32_t(tiles < uint64_t(dev_blocks) ? tiles : uint64_t(dev_blocks));
     auto *hdr = reinterpret_cast<ScratchHeader *>(scratch);
     auto *desc = reinterpret_cast<uint64_t *>(static_cast<unsigned char *>(scratch) + kHeaderBytes);
-    kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(
-        reinterpret_cast<const typename Op::T *>(in), reinterpret_cast<typename Op::T *>(out), n,
-        uint32_t(tiles), hdr, desc, fault);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(C::kThreads), C::kSmemBytes, stream,
+                      reinterpret_cast<const typename Op::T *>(in),
+                      reinterpret_cast<typename Op::T *>(out), n, uint32_t(tiles), hdr, desc, fault);
 }
 
 }  // namespace
@@ -633,6 +634,7 @@ cudaError_t launch_scan(dwp_op op, bool inclusive, const void *in, void *out, ui
     LaunchKnobs fault = current_launch_knobs();
     // in place, the input of a stalled tile may already be output: no fallback
     if (in == out) fault.fallback_polls = 0u;
+    if (n <= kScanSmallMax) return launch_scan_small(op, inclusive, in, out, n, scratch, stream, fault);
     switch (op) {
         case DWP_U32_ADD:
             return inclusive ? launch_one<OpU32Add, true>(in, out, n, scratch, stream, fault)

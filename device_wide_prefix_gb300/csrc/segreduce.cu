@@ -91,6 +91,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         fence_mbar_init();
     }
     __syncwarp();
+    // shared memory only so far; the kernel before may still be running.
+    // No early trigger: the next kernel launches as the blocks exit (an
+    // early one measured slower for this persistent kernel)
+    pdl_wait();
 
     // take a tile index and start its bulk copy into stage j (lane 0 only)
     auto start = [&](int j) -> uint32_t {
@@ -230,9 +234,8 @@ cudaError_t launch_segreduce(const uint32_t *values, const uint32_t *offsets, ui
     const uint32_t grid = uint32_t(blocks_needed < uint64_t(dev_blocks) ? blocks_needed
                                                                          : uint64_t(dev_blocks));
     auto *hdr = reinterpret_cast<ScratchHeader *>(scratch);
-    kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(values, offsets, nseg, out, n,
-                                                        uint32_t(tiles), hdr);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(C::kThreads), C::kSmemBytes, stream, values, offsets,
+                      nseg, out, n, uint32_t(tiles), hdr);
 }
 
 }  // namespace dwp

@@ -208,7 +208,11 @@ struct SegRescue {
     }
 };
 
-template <bool INCL, class C>
+// PERTURB compiles in the schedule-perturbation points of the test hook
+// dwp_debug_set_delay.  Launches pick the variant without them unless the
+// hook is on: in this kernel the inlined points alone (never taken) cost
+// measurable time, so production launches carry none of their code.
+template <bool INCL, class C, bool PERTURB>
 __global__ void __launch_bounds__(C::kThreads, 1)
     segscan_kernel(const uint32_t *in, const uint32_t *off, uint32_t nseg, uint32_t *out,
                    uint64_t n, uint32_t num_tiles, ScratchHeader *hdr, uint64_t *desc,
@@ -225,6 +229,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const SegSmem<C> sm(smem_raw);
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
+    // the kernel before may still be running: wait before reading anything
+    // (no early trigger, as in the plain scan: the next kernel launches as
+    // the blocks exit)
+    pdl_wait();
 
     // offset sample: sample[i] = off[min(i * stride, N)]
     const uint64_t noff = uint64_t(nseg) + 1;
@@ -287,7 +295,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 if (ld_volatile_smem(sm.abort_flag()) == 0) {
                     t = atomicAdd(&hdr->tile_counter, 1u);
                     if (t >= num_tiles) t = kNoTile;
-                    else perturb(fault, t, kSiteDraw);
+                    else if (PERTURB) perturb(fault, t, kSiteDraw);
                 }
                 *reinterpret_cast<volatile uint32_t *>(sm.tile_id(gi)) = t;
                 ++taken;
@@ -419,7 +427,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 // ragged last tile too); element by element only for the
                 // thread holding the 1-3 elements after the bulk part; heads
                 // lie below the tile end, so threads past it hold nothing
-                const bool vec = c * ITEMS + ITEMS <= bulk;
+                const bool vec = valid == uint32_t(TILE) || c * ITEMS + ITEMS <= bulk;
                 if (vec && !hb) {
                     const uint4 *v4 = reinterpret_cast<const uint4 *>(buf);
 #pragma unroll
@@ -495,7 +503,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 pre[prefix_slot(lane * PER + j)] = hj ? mv[j] : ev + mv[j];
                 if (tile_heads) ph[lane * PER + j] = (hj | eh) ? 1 : 0;
             }
-            perturb(fault, t, kSiteAggregate);
+            if (PERTURB) perturb(fault, t, kSiteAggregate);
             if (lane == 0) {
                 if (t != fault.never_publish_tile)
                     st_relaxed_gpu(desc + t, make_desc((t == 0 || ah) ? kPrefix : kAggregate, av));
@@ -531,14 +539,14 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             uint32_t carry = 0;
             int rc = (draining || ld_volatile_smem(sm.lbres(i)) != 0u) ? 1 : 0;
             const bool ah = ld_volatile_smem(sm.agg_head(i)) != 0u;
-            if (rc == 0) perturb(fault, t, kSiteLookback);
+            if (PERTURB && rc == 0) perturb(fault, t, kSiteLookback);
             if (rc == 0 && t != 0 && ld_volatile_smem(sm.first_head(i)) == 0u)
                 rc = lookback<Op, C::kLookK>(desc, t, lane, fault.spin_limit, fault.fallback_polls,
                                              SegRescue{in, off, nseg, n, uint32_t(TILE)},
                                              hdr, fault.lookback_window, *sm.agg(i),
                                              !ah && t != fault.never_publish_tile, sm.lb_scratch(i),
                                              &carry);
-            if (rc == 0) perturb(fault, t, kSitePrefix);
+            if (PERTURB && rc == 0) perturb(fault, t, kSitePrefix);
             if (lane == 0) {
                 if (rc == 0) {
                     if (t != 0 && !ah && t != fault.never_publish_tile)
@@ -636,7 +644,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         uint32_t acc = phd ? pv : *sm.carry(i) + pv;
         __syncwarp();
         if (lane == 0) mbar_arrive(sm.info_free(i));  // the info slot has been read
-        if (covered && p0 + ITEMS <= bulk) {
+        if (covered && (valid == uint32_t(TILE) || p0 + ITEMS <= bulk)) {
             uint4 *v4 = reinterpret_cast<uint4 *>(buf + p0);
 #pragma unroll
             for (int v = 0; v < ITEMS / 4; ++v) {
@@ -704,7 +712,7 @@ cudaError_t launch_seg(const uint32_t *values, const uint32_t *offsets, uint32_t
                        uint32_t *out, uint64_t n, void *scratch, cudaStream_t stream,
                        const LaunchKnobs &fault) {
     using C = SegCfg;
-    auto kern = segscan_kernel<INCL, C>;
+    auto kern = fault.delay_threshold != 0u ? segscan_kernel<INCL, C, true> : segscan_kernel<INCL, C, false>;
     const int dev_blocks = device_blocks(reinterpret_cast<const void *>(kern), C::kThreads,
                                          C::kSmemBytes);
     if (dev_blocks <= 0) return cudaErrorInvalidConfiguration;
@@ -712,9 +720,8 @@ cudaError_t launch_seg(const uint32_t *values, const uint32_t *offsets, uint32_t
     const uint32_t grid = uint32_t(tiles < uint64_t(dev_blocks) ? tiles : uint64_t(dev_blocks));
     auto *hdr = reinterpret_cast<ScratchHeader *>(scratch);
     auto *desc = reinterpret_cast<uint64_t *>(static_cast<unsigned char *>(scratch) + kHeaderBytes);
-    kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(values, offsets, nseg, out, n,
-                                                       uint32_t(tiles), hdr, desc, fault);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(C::kThreads), C::kSmemBytes, stream, values, offsets,
+                      nseg, out, n, uint32_t(tiles), hdr, desc, fault);
 }
 
 }  // namespace

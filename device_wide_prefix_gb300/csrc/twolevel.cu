@@ -54,6 +54,8 @@ __device__ __forceinline__ typename Op::T warp_incl_scan(typename Op::T v, uint3
 // of the five steps to out[width * k + l].
 __global__ void warp_scan_trace_kernel(const uint32_t *x, uint32_t width, uint32_t *out) {
     __shared__ uint32_t steps[5 * 32];
+    pdl_wait();
+    pdl_trigger();
     const uint32_t lane = threadIdx.x & 31u;
     const uint32_t v = lane < width ? x[lane] : OpU32Add::identity();
     warp_incl_scan<OpU32Add>(v, lane, steps);
@@ -113,6 +115,8 @@ __global__ void __launch_bounds__(kTlThreads) tl_reduce(const typename Op::T *in
                                                         uint32_t *totals) {
     using T = typename Op::T;
     __shared__ uint32_t warp_tot[33];
+    pdl_wait();
+    pdl_trigger();
     const uint64_t first = uint64_t(blockIdx.x) * kTlChunk + uint64_t(threadIdx.x) * kTlItems;
     T v[kTlItems];
     load_items<Op>(in, n, first, v);
@@ -128,6 +132,8 @@ template <class Op>
 __global__ void __launch_bounds__(kTlTotThreads) tl_scan_totals(uint32_t *totals, uint32_t count) {
     using T = typename Op::T;
     __shared__ uint32_t warp_tot[33];
+    pdl_wait();
+    pdl_trigger();
     const uint32_t first = threadIdx.x * kTlTotItems;
     T v[kTlTotItems];
     T acc = Op::identity();
@@ -150,6 +156,8 @@ __global__ void __launch_bounds__(kTlThreads) tl_scan(const typename Op::T *in, 
                                                       uint64_t n, const uint32_t *totals) {
     using T = typename Op::T;
     __shared__ uint32_t warp_tot[33];
+    pdl_wait();
+    pdl_trigger();
     const uint64_t first = uint64_t(blockIdx.x) * kTlChunk + uint64_t(threadIdx.x) * kTlItems;
     T v[kTlItems];
     load_items<Op>(in, n, first, v);
@@ -189,10 +197,15 @@ cudaError_t launch_tl(const void *in, void *out, uint64_t n, void *scratch, cuda
     const uint64_t blocks = (n + kTlChunk - 1) / kTlChunk;
     auto *totals = reinterpret_cast<uint32_t *>(static_cast<unsigned char *>(scratch) + kHeaderBytes);
     const T *src = static_cast<const T *>(in);
-    tl_reduce<Op><<<uint32_t(blocks), kTlThreads, 0, stream>>>(src, n, totals);
-    tl_scan_totals<Op><<<1, kTlTotThreads, 0, stream>>>(totals, uint32_t(blocks));
-    tl_scan<Op, INCL><<<uint32_t(blocks), kTlThreads, 0, stream>>>(src, static_cast<T *>(out), n, totals);
-    return cudaGetLastError();
+    cudaError_t e = launch_pdl(tl_reduce<Op>, dim3(uint32_t(blocks)), dim3(kTlThreads), 0, stream,
+                               src, n, totals);
+    if (e == cudaSuccess)
+        e = launch_pdl(tl_scan_totals<Op>, dim3(1), dim3(kTlTotThreads), 0, stream, totals,
+                       uint32_t(blocks));
+    if (e == cudaSuccess)
+        e = launch_pdl(tl_scan<Op, INCL>, dim3(uint32_t(blocks)), dim3(kTlThreads), 0, stream, src,
+                       static_cast<T *>(out), n, static_cast<const uint32_t *>(totals));
+    return e;
 }
 
 }  // namespace
@@ -221,8 +234,11 @@ cudaError_t launch_two_level(dwp_op op, bool inclusive, const void *in, void *ou
 extern "C" dwp_status dwp_debug_warp_scan_trace(const uint32_t *d_x, size_t width, uint32_t *d_steps,
                                                 dwp_stream stream) {
     if (width == 0 || width > 32 || !d_x || !d_steps) return DWP_ERR_INVALID_VALUE;
-    dwp::warp_scan_trace_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        d_x, uint32_t(width), d_steps);
-    if (cudaGetLastError() != cudaSuccess) return DWP_ERR_CUDA;
+    if (dwp::launch_pdl(dwp::warp_scan_trace_kernel, dim3(1), dim3(32), 0,
+                        reinterpret_cast<cudaStream_t>(stream), d_x, uint32_t(width),
+                        d_steps) != cudaSuccess) {
+        cudaGetLastError();
+        return DWP_ERR_CUDA;
+    }
     return DWP_SUCCESS;
 }
