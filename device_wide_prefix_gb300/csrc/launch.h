@@ -43,14 +43,17 @@ int device_blocks(const void *kernel, int threads, size_t smem_bytes);
 // (scan_small.cu: one block per tile, registers only); larger ones the
 // persistent pipelined kernel (scan.cu).
 constexpr uint64_t kScanSmallMax = uint64_t(1) << 22;
-// Elements per tile of the two plain scan kernels (the small-input one
-// sizes its tile by n).
+// Elements per tile of the large-input plain scan kernel.
 uint32_t scan_tile_elems();
-uint32_t scan_small_tile_elems(uint64_t n);
-// Tiles, so descriptors, the plain scan uses for n elements.
+// Descriptors the small-input kernel needs for n <= kScanSmallMax: at least
+// its tile count, and never fewer than for any smaller n (it sizes its tile
+// by n, so its tile count alone is not monotone in n).
+uint64_t scan_small_descriptors(uint64_t n);
+// Descriptors the plain scan's size query asks for: non-decreasing in n, so
+// scratch sized for the largest n serves every smaller one.
 inline uint64_t scan_tiles(uint64_t n) {
-    const uint64_t tile = n <= kScanSmallMax ? scan_small_tile_elems(n) : scan_tile_elems();
-    return (n + tile - 1) / tile;
+    return n <= kScanSmallMax ? scan_small_descriptors(n)
+                              : (n + scan_tile_elems() - 1) / scan_tile_elems();
 }
 // One launch of the plain scan (the scratch has already been cleared); picks
 // the kernel by n as above.

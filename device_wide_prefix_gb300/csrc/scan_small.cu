@@ -252,8 +252,12 @@ cudaError_t launch_small(const void *in, void *out, uint64_t n, void *scratch, c
 
 }  // namespace
 
-uint32_t scan_small_tile_elems(uint64_t n) {
-    return n <= kSmallSplit ? SmallSmem<12>::kTile : SmallSmem<60>::kTile;
+uint64_t scan_small_descriptors(uint64_t n) {
+    constexpr uint64_t t12 = SmallSmem<12>::kTile, t60 = SmallSmem<60>::kTile;
+    if (n <= kSmallSplit) return (n + t12 - 1) / t12;
+    const uint64_t at_split = (kSmallSplit + t12 - 1) / t12;  // 86
+    const uint64_t tiles = (n + t60 - 1) / t60;
+    return tiles > at_split ? tiles : at_split;
 }
 
 cudaError_t launch_scan_small(dwp_op op, bool inclusive, const void *in, void *out, uint64_t n,

@@ -204,8 +204,7 @@ dwp_status dwp_read_static_status(dwp_stream stream);
  * comparison with the single-pass scan.
  *   n            at most 2^26 (DWP_ERR_INVALID_VALUE above).
  *   d_scratch    NULL: *scratch_bytes receives the size needed (128 bytes
- *                plus 4 bytes per 4096-element block).  Never more than
- *                dwp_scan_exclusive asks for the same n.
+ *                plus 4 bytes per 4096-element block).
  * Pointers, alignment, in-place use and errors as for dwp_scan_exclusive.
  */
 dwp_status dwp_scan_two_level(dwp_op op, dwp_mode mode, const void *d_in, void *d_out, size_t n,

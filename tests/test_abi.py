@@ -60,20 +60,23 @@ def test_scan_size_query(lib):
                 if tile is None:
                     tile = n if n > 1 else None
                 assert tiles >= 1
-    # one descriptor per tile: the tile size T is the largest n that needs one
-    _, b1 = dwp.dwp_scan_exclusive(dwp.DWP_U32_ADD, 0, 0, 1, 0, 0, 0)
-    T = 1
-    while dwp.dwp_scan_exclusive(dwp.DWP_U32_ADD, 0, 0, 2 * T, 0, 0, 0)[1] == b1:
-        T *= 2
-    lo, hi = T, 2 * T  # T needs one descriptor, 2T needs two
-    while hi - lo > 1:
-        mid = (lo + hi) // 2
-        if dwp.dwp_scan_exclusive(dwp.DWP_U32_ADD, 0, 0, mid, 0, 0, 0)[1] == b1:
-            lo = mid
-        else:
-            hi = mid
-    T = lo
-    for k in (1, 7, 1000):
+    # scratch sized for a large n serves every smaller n: the size query
+    # never decreases (the small-input kernel sizes its tile by n)
+    prev = 0
+    for n in sorted({1, 2, 3071, 3072, 3073, (1 << 18) - 1, 1 << 18, (1 << 18) + 1, 15360 * 20,
+                     15360 * 86, 15360 * 86 + 1, (1 << 22) - 1, 1 << 22, (1 << 22) + 1, 1 << 24,
+                     (1 << 28) + 5, (1 << 32) - 1}):
+        b = dwp.dwp_scan_exclusive(dwp.DWP_U32_ADD, 0, 0, n, 0, 0, 0)[1]
+        assert b >= prev, n
+        prev = b
+    # above 2^22 one descriptor per tile of the large-input kernel; its tile
+    # size T follows from a large query
+    big = 1 << 30
+    tiles = (dwp.dwp_scan_exclusive(dwp.DWP_U32_ADD, 0, 0, big, 0, 0, 0)[1] - 128) // 8
+    T = -(-big // tiles)
+    assert -(-big // T) == tiles
+    for k in (1000, 7777):
+        assert k * T > 1 << 22
         assert dwp.dwp_scan_exclusive(dwp.DWP_U32_ADD, 0, 0, k * T, 0, 0, 0)[1] == 128 + 8 * k
         assert dwp.dwp_scan_exclusive(dwp.DWP_U32_ADD, 0, 0, k * T + 1, 0, 0, 0)[1] == 128 + 8 * (k + 1)
 
@@ -182,9 +185,9 @@ def test_two_level_size_query_and_validation(lib):
     assert R(dwp.DWP_U32_ADD, dwp.DWP_EXCLUSIVE, 0, 0, 1, 0, 0, 0) == (dwp.DWP_SUCCESS, 132)
     assert R(dwp.DWP_U32_ADD, dwp.DWP_EXCLUSIVE, 0, 0, 4096 * 4, 0, 0, 0) == (dwp.DWP_SUCCESS, 144)
     assert R(dwp.DWP_U32_ADD, dwp.DWP_EXCLUSIVE, 0, 0, 4096 * 4 + 1, 0, 0, 0) == (dwp.DWP_SUCCESS, 148)
-    # never more than the single-pass scan asks for
-    for n in (1, 4096, 4097, 7168, 7169, 12000, 1 << 20, (1 << 26) - 1, 1 << 26):
-        assert R(0, 0, 0, 0, n, 0, 0, 0)[1] <= dwp.dwp_scan_exclusive(0, 0, 0, n, 0, 0, 0)[1], n
+    # a 4-byte total per 4096-element block
+    for n in (4096, 4097, 7168, 12000, 1 << 20, (1 << 26) - 1):
+        assert R(0, 0, 0, 0, n, 0, 0, 0)[1] == 128 + 4 * (-(-n // 4096)), n
     assert R(dwp.DWP_U32_ADD, dwp.DWP_EXCLUSIVE, 0, 0, 1 << 26, 0, 0, 0) == (dwp.DWP_SUCCESS, 128 + 4 * 16384)
     assert R(dwp.DWP_U32_ADD, dwp.DWP_EXCLUSIVE, 0, 0, (1 << 26) + 1, 0, 0, 0)[0] == dwp.DWP_ERR_INVALID_VALUE
     n, need = 1000, 132

@@ -57,9 +57,10 @@ def check(ref, x, op, inclusive, y):
 
 
 def test_small_kernel_tiles_in_the_size_query():
-    """One descriptor per 3072 elements up to 2^18, per 15360 up to 2^22."""
-    for n, tiles in ((1, 1), (T, 1), (T + 1, 2), (1 << 18, 86), ((1 << 18) + 1, 18),
-                     (SMALL_MAX, 274)):
+    """One descriptor per 3072 elements up to 2^18; above, one per 15360
+    elements but never fewer than at 2^18 (the size query does not shrink)."""
+    for n, tiles in ((1, 1), (T, 1), (T + 1, 2), (1 << 18, 86), ((1 << 18) + 1, 86),
+                     (86 * T2 + 1, 87), (SMALL_MAX, 274)):
         assert dwp.scan_scratch_bytes(n) == 128 + 8 * tiles
 
 
