@@ -42,6 +42,15 @@ METRIC = "u32 exclusive scan Gelem/s and HBM GB/s as % of peak at n=2^28; segsca
 N_FULL = 1 << 28
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "scan_u32_exclusive_2p28.md")
 KERNEL_SOURCES = ["device_wide_prefix_gb300/csrc/scan.cu", "device_wide_prefix_gb300/csrc/device.cuh"]
+CSRC = "device_wide_prefix_gb300/csrc/"
+# ncu summary and kernel sources behind each secondary entry's traffic figure
+SECONDARY_PROFILES = {
+    "segscan_u32_exclusive": ("segscan_u32_skewed.md", [CSRC + "segscan.cu", CSRC + "device.cuh"]),
+    "compact_16B_records": ("compact_16B_records.md", [CSRC + "compact.cu", CSRC + "device.cuh"]),
+    "linear_recurrence_f32": ("recurrence_f32_2p28.md", [CSRC + "recurrence.cu", CSRC + "device.cuh"]),
+    "segreduce_u32": ("segreduce_u32_skewed.md", [CSRC + "segreduce.cu", CSRC + "device.cuh"]),
+    "u32_add_exclusive_2p20": ("scan_small_u32_2p20.md", [CSRC + "scan_small.cu", CSRC + "device.cuh"]),
+}
 
 
 def kernel_hash(paths=KERNEL_SOURCES) -> str:
@@ -210,7 +219,7 @@ def main() -> None:
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=10.0)
     ap.add_argument("--only", default=None,
-                    choices=["segscan", "compact", "recurrence", "segreduce", "compact_staged"],
+                    choices=["scan", "segscan", "compact", "recurrence", "segreduce", "compact_staged"],
                     help="time only this workload (at --log2n) and print its entry; for "
                          "profiler captures")
     ap.add_argument("--log2n", type=int, default=28,
@@ -485,6 +494,9 @@ def measure_secondary(dwp, lib, dev, stream, peaks, x, y, scratch, need) -> dict
     out["compact_staged_vs_fused"] = measure_compact_staged(dwp, lib, dev, stream, peaks)
     out["linear_recurrence_f32"] = measure_recurrence(dwp, lib, dev, stream, peaks)
     out["segreduce_u32"] = measure_segreduce(dwp, lib, dev, stream, peaks)
+    for name, (summary, sources) in SECONDARY_PROFILES.items():
+        if name in out:
+            out[name]["traffic"] = profiled_traffic(os.path.join(ROOT, "profiles", summary), sources)
     return out
 
 
@@ -596,12 +608,34 @@ def run_only(args) -> None:
     dev = torch.device("cuda", 0)
     lib = dwp.load()
     stream = torch.cuda.current_stream(dev)
-    fn = {"segscan": measure_segscan, "compact": measure_compact,
+    fn = {"scan": measure_scan_only, "segscan": measure_segscan, "compact": measure_compact,
           "recurrence": measure_recurrence, "segreduce": measure_segreduce,
           "compact_staged": measure_compact_staged}[args.only]
     r = fn(dwp, lib, dev, stream, measured_peaks(), log2n=args.log2n, steps=args.steps,
            warmup=args.warmup)
     print(json.dumps({"only": args.only, **r}), flush=True)
+
+
+def measure_scan_only(dwp, lib, dev, stream, peaks, log2n=28, steps=100, warmup=5) -> dict:
+    """u32 exclusive add scan of 2^log2n full-range values alone (the kernel
+    the size picks: small-input up to 2^22, pipelined above)."""
+    import ctypes
+    import torch
+    n = 1 << log2n
+    x = torch.from_numpy(synth.u32_full_values(n).view(np.int32)).to(dev)
+    y = torch.empty_like(x)
+    need = dwp.scan_scratch_bytes(n)
+    scratch = dwp.alloc_scratch(need, dev)
+    sb = ctypes.c_size_t(need)
+    args = (dwp.DWP_U32_ADD, ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(y.data_ptr()), n,
+            ctypes.c_void_p(scratch.data_ptr()), ctypes.byref(sb), ctypes.c_void_p(int(stream.cuda_stream)))
+    stats = {}
+    ms = time_calls(lambda: lib.dwp_scan_exclusive(*args), steps, warmup, stream, stats)
+    if dwp.read_status(scratch) != dwp.DWP_SUCCESS:
+        raise RuntimeError("scan reported a device-side error")
+    gbs = 8 * n / (ms * 1e-3) / 1e9
+    return {"n": n, "ms": ms, **stats, "Gelem_s": n / (ms * 1e-3) / 1e9, "GB_s": gbs,
+            "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": 8 * n}
 
 
 def measure_compact(dwp, lib, dev, stream, peaks, log2n=26, steps=100, warmup=5) -> dict:

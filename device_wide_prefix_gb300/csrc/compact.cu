@@ -85,6 +85,13 @@ struct CompactConfig {
 #ifndef DWP_CMP_LOOKK
 #define DWP_CMP_LOOKK 1
 #endif
+// Where the L2 prefetch of a tile's records is issued: 0 none, 1 by the
+// producer when it draws the tile, 2 by the tile warp once the tile's count
+// is published, 3 once its look-back is done (later points leave fewer
+// prefetched lines waiting in L2 at once).
+#ifndef DWP_CMP_PREFETCH
+#define DWP_CMP_PREFETCH 2
+#endif
 using CmpCfg = CompactConfig<DWP_CMP_WARPS, DWP_CMP_ITEMS, DWP_CMP_OUT, DWP_CMP_RING,
                              DWP_CMP_TILEWARPS, DWP_CMP_LOOKK>;
 
@@ -121,6 +128,13 @@ struct CmpSmem {
     }
     __device__ uint32_t *end_iter() const { return abort_flag() + 1; }
 };
+
+// Bit j (j < 4) set when byte j of x is nonzero: the compare gives 0xff per
+// nonzero byte; the multiply gathers the low bit of each byte into bits
+// 24..27 (no partial product reaches them but these four).
+__device__ __forceinline__ uint32_t nonzero_bytes4(uint32_t x) {
+    return ((__vcmpne4(x, 0u) & 0x01010101u) * 0x01020408u) >> 24;
+}
 
 // Keep flag of record pos of a tile: from the slot below `fbulk`, from global
 // memory below `valid`, else 0.
@@ -230,7 +244,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             uint32_t valid, fbulk;
             tile_extent(t, valid, fbulk);
             const uint64_t base = uint64_t(t) * TILE;
-            bulk_prefetch_l2(recs + base, valid * 16u, keep);
+            if (DWP_CMP_PREFETCH == 1) bulk_prefetch_l2(recs + base, valid * 16u, keep);
             if (fbulk) {
                 mbar_arrive_expect_tx(sm.flags_full(i), fbulk);
                 bulk_load(sm.flags(i), flags + base, fbulk, sm.flags_full(i));
@@ -272,30 +286,52 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             const unsigned char *sf = sm.flags(i);
             uint32_t *pre = sm.prefix(i);
             uint32_t *lt = sm.lane_tot(i);
-            // K1: kept count of consumer thread c = lane + 32w (records c*IT ..)
-#pragma unroll
-            for (int w2 = 0; w2 < NW; ++w2) {
-                const uint32_t c = lane + 32u * w2;
-                uint32_t cnt = 0;
-                // straight from the slot wherever all IT flags were
-                // bulk-copied (a ragged last tile too); flag by flag only for
-                // the threads holding the (at most 15) flags after the bulk part
-                if (c * IT + IT <= fbulk) {
-#pragma unroll
-                    for (int q = 0; q < IT; ++q) cnt += sf[c * IT + q] != 0;
-                } else if (c * IT < valid) {
-                    for (int q = 0; q < IT; ++q) cnt += keep_at(sf, flags, base, c * IT + q, fbulk, valid);
-                }
-                pre[prefix_slot(c)] = cnt;
-            }
-            __syncwarp();
-            // K2: exclusive prefix of the counts (lane l: threads PER*l ..)
+            // K1: lane l takes consumer threads PER*l .. PER*l + PER-1, whose
+            // flags are the PER*IT contiguous bytes from PER*IT*l: read as
+            // 16-byte vectors (a lane stride of 80 bytes, 5 times 16, so a
+            // quarter warp hits 8 distinct bank groups), the keep mask and
+            // count of each thread worked out in registers.  A ragged last
+            // tile reads its flags one by one.
             constexpr int PER = NCONS / 32;
+            static_assert(IT <= 5 && (PER * IT) % 16 == 0, "a thread's flags sit in one 8-byte window");
+            static_assert(TILE < (1 << 24), "prefixes share a word with an 8-bit keep mask");
+            uint32_t cntm[PER];  // kept count | keep mask << 24
+            if (valid == uint32_t(TILE)) {
+                const uint4 *fv = reinterpret_cast<const uint4 *>(sf) + lane * (PER * IT / 16);
+                uint32_t wd[PER * IT / 4 + 1];
+#pragma unroll
+                for (int q = 0; q < PER * IT / 16; ++q) {
+                    const uint4 x = fv[q];
+                    wd[4 * q + 0] = x.x;
+                    wd[4 * q + 1] = x.y;
+                    wd[4 * q + 2] = x.z;
+                    wd[4 * q + 3] = x.w;
+                }
+                wd[PER * IT / 4] = 0u;
+#pragma unroll
+                for (int j = 0; j < PER; ++j) {
+                    const int lo = j * IT, w = lo >> 2, sh = (lo & 3) * 8;
+                    const uint64_t v = ((uint64_t(wd[w + 1]) << 32) | wd[w]) >> sh;
+                    const uint32_t m = (nonzero_bytes4(uint32_t(v)) | (nonzero_bytes4(uint32_t(v >> 32)) << 4)) &
+                                       ((1u << IT) - 1u);
+                    cntm[j] = uint32_t(__popc(m)) | (m << 24);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < PER; ++j) {
+                    const uint32_t p0 = (lane * PER + j) * IT;
+                    uint32_t m = 0;
+                    for (int q = 0; q < IT; ++q)
+                        if (keep_at(sf, flags, base, p0 + q, fbulk, valid)) m |= 1u << q;
+                    cntm[j] = uint32_t(__popc(m)) | (m << 24);
+                }
+            }
+            // K2: exclusive prefix of the counts, lane by lane
             uint32_t mine[PER], run = 0;
 #pragma unroll
             for (int q = 0; q < PER; ++q) {
                 mine[q] = run;
-                run += pre[prefix_slot(lane * PER + q)];
+                run += cntm[q] & 0xffffffu;
             }
             lt[lane] = run;
             __syncwarp();
@@ -306,11 +342,15 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 if (uint32_t(l) < lane) lane_excl += v;
                 total += v;
             }
+            // each thread's exclusive prefix, its keep mask in the top byte
 #pragma unroll
-            for (int q = 0; q < PER; ++q) pre[prefix_slot(lane * PER + q)] = lane_excl + mine[q];
+            for (int q = 0; q < PER; ++q)
+                pre[prefix_slot(lane * PER + q)] = (lane_excl + mine[q]) | (cntm[q] & 0xff000000u);
             perturb(fault, t, kSiteAggregate);
             if (lane == 0 && t != fault.never_publish_tile)
                 st_relaxed_gpu(desc + t, make_desc(t == 0 ? kPrefix : kAggregate, total));
+            if (DWP_CMP_PREFETCH == 2 && lane == 0 && total != 0u)
+                bulk_prefetch_l2(recs + base, valid * 16u, l2_policy_evict_last());
             uint32_t carry = 0;
             int rc = 0;
             perturb(fault, t, kSiteLookback);
@@ -320,6 +360,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                                              fault.lookback_window, total,
                                              t != fault.never_publish_tile, sm.lb_scratch(i), &carry);
             if (rc == 0) perturb(fault, t, kSitePrefix);
+            if (DWP_CMP_PREFETCH == 3 && lane == 0 && rc == 0 && total != 0u)
+                bulk_prefetch_l2(recs + base, valid * 16u, l2_policy_evict_last());
             if (lane == 0) {
                 if (rc == 0) {
                     if (t != 0 && t != fault.never_publish_tile)
@@ -396,22 +438,21 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             const uint64_t base = uint64_t(t) * TILE;
             uint4 *region = sm.recs(o) + cw * WR;
             const uint32_t *pre = sm.prefix(i);
-            const uint32_t wfirst = pre[prefix_slot(cw * 32)];
-            const uint32_t wend =
-                cw + 1 < uint32_t(NW) ? pre[prefix_slot(cw * 32 + 32)] : *sm.tile_count(i);
+            const uint32_t wfirst = pre[prefix_slot(cw * 32)] & 0xffffffu;
+            const uint32_t wend = cw + 1 < uint32_t(NW) ? pre[prefix_slot(cw * 32 + 32)] & 0xffffffu
+                                                        : *sm.tile_count(i);
             nkeep = wend - wfirst;
             first = *sm.carry(i) + wfirst;
-            // K3: read this thread's records, then (after the whole warp has
-            // read) write the kept ones to their in-warp slots, in order
+            // K3: read this thread's kept records (the keep mask rides in the
+            // top byte of its prefix word), then (after the whole warp has
+            // read) write them to their in-warp slots, in order
+            const uint32_t pv = pre[prefix_slot(c)];
+            const uint32_t keepm = pv >> 24;
             uint4 r[IT];
-            uint32_t keepm = 0;
 #pragma unroll
-            for (int q = 0; q < IT; ++q) {
-                const uint32_t pos = c * IT + q;
-                if (pos < valid) r[q] = sm.recs(o)[pos];
-                if (keep_at(sm.flags(i), flags, base, pos, fbulk, valid)) keepm |= 1u << q;
-            }
-            uint32_t slot = pre[prefix_slot(c)] - wfirst;
+            for (int q = 0; q < IT; ++q)
+                if ((keepm >> q) & 1u) r[q] = sm.recs(o)[c * IT + q];
+            uint32_t slot = (pv & 0xffffffu) - wfirst;
             __syncwarp();
 #pragma unroll
             for (int q = 0; q < IT; ++q)
