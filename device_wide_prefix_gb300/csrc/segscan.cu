@@ -415,9 +415,13 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 return;
             }
             // -- per-thread (head, value) totals ---------------------------
+            // Totals and head bits stay in registers until the stage is
+            // freed: a shared-memory store between the loads would keep the
+            // compiler from having the next rows' loads in flight.
             const uint32_t *buf = sm.in_data(s);
             uint32_t *pre = sm.prefix(i);
             unsigned char *ph = sm.phead(i);
+            uint32_t tot[NW], thb[NW];
 #pragma unroll
             for (int w2 = 0; w2 < NW; ++w2) {
                 const uint32_t c = lane + 32u * w2;
@@ -453,12 +457,19 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                         acc = ((hb >> j) & 1u) ? x : acc + x;
                     }
                 }
-                pre[prefix_slot(c)] = acc;
-                if (tile_heads) ph[c] = hb ? 1 : 0;
+                tot[w2] = acc;
+                thb[w2] = hb;
             }
             // the input stage is no longer needed
             __syncwarp();
             if (lane == 0) mbar_arrive(sm.in_empty(s));
+#pragma unroll
+            for (int w2 = 0; w2 < NW; ++w2) {
+                const uint32_t c = lane + 32u * w2;
+                pre[prefix_slot(c)] = tot[w2];
+                if (tile_heads) ph[c] = thb[w2] ? 1 : 0;
+            }
+            __syncwarp();
             // lane l scans threads PER*l .. PER*l+PER-1 with the pair operator
             constexpr int PER = NCONS / 32;
             uint32_t mv[PER], mh = 0, rv = 0, rh = 0;
