@@ -40,9 +40,13 @@ cudaError_t launch_clear(void *a, size_t a_bytes, void *b, size_t b_bytes, cudaS
 int device_blocks(const void *kernel, int threads, size_t smem_bytes);
 
 // Inputs of at most this many elements take the small-input plain scan
-// (scan_small.cu: one block per tile, registers only); larger ones the
-// persistent pipelined kernel (scan.cu).
-constexpr uint64_t kScanSmallMax = uint64_t(1) << 22;
+// (scan_small.cu: one block per tile); larger ones the persistent pipelined
+// kernel (scan.cu).  Measured on GB300: at 2^23 the small-input kernel takes
+// 19.3 us and the pipelined one 22.8; at 2^24, 43.3 against 34.4.
+#ifndef DWP_SCAN_SMALL_LOG2
+#define DWP_SCAN_SMALL_LOG2 23
+#endif
+constexpr uint64_t kScanSmallMax = uint64_t(1) << DWP_SCAN_SMALL_LOG2;
 // Elements per tile of the large-input plain scan kernel.
 uint32_t scan_tile_elems();
 // Descriptors the small-input kernel needs for n <= kScanSmallMax: at least

@@ -240,7 +240,7 @@ cudaError_t launch_small_items(const void *in, void *out, uint64_t n, void *scra
 }
 
 // Up to 2^18 elements a tile is 256 * 12 = 3072 elements (at most 86
-// tiles); above, 256 * 60 = 15360 (at most 274 tiles up to 2^22).
+// tiles); above, 256 * 60 = 15360 (at most 547 tiles up to 2^23).
 constexpr uint64_t kSmallSplit = uint64_t(1) << 18;
 
 template <class Op, bool INCL>

@@ -64,19 +64,20 @@ def test_scan_size_query(lib):
     # never decreases (the small-input kernel sizes its tile by n)
     prev = 0
     for n in sorted({1, 2, 3071, 3072, 3073, (1 << 18) - 1, 1 << 18, (1 << 18) + 1, 15360 * 20,
-                     15360 * 86, 15360 * 86 + 1, (1 << 22) - 1, 1 << 22, (1 << 22) + 1, 1 << 24,
+                     15360 * 86, 15360 * 86 + 1, (1 << 22) - 1, 1 << 22, (1 << 22) + 1,
+                     (1 << 23) - 1, 1 << 23, (1 << 23) + 1, 1 << 24,
                      (1 << 28) + 5, (1 << 32) - 1}):
         b = dwp.dwp_scan_exclusive(dwp.DWP_U32_ADD, 0, 0, n, 0, 0, 0)[1]
         assert b >= prev, n
         prev = b
-    # above 2^22 one descriptor per tile of the large-input kernel; its tile
+    # above 2^23 one descriptor per tile of the large-input kernel; its tile
     # size T follows from a large query
     big = 1 << 30
     tiles = (dwp.dwp_scan_exclusive(dwp.DWP_U32_ADD, 0, 0, big, 0, 0, 0)[1] - 128) // 8
     T = -(-big // tiles)
     assert -(-big // T) == tiles
-    for k in (1000, 7777):
-        assert k * T > 1 << 22
+    for k in (2000, 7777):
+        assert k * T > 1 << 23
         assert dwp.dwp_scan_exclusive(dwp.DWP_U32_ADD, 0, 0, k * T, 0, 0, 0)[1] == 128 + 8 * k
         assert dwp.dwp_scan_exclusive(dwp.DWP_U32_ADD, 0, 0, k * T + 1, 0, 0, 0)[1] == 128 + 8 * (k + 1)
 

@@ -1,5 +1,5 @@
 """Parity of the small-input plain scan (one block per tile of 3072 elements
-up to n = 2^18, of 15360 elements up to n = 2^22) with the sequential
+up to n = 2^18, of 15360 elements up to n = 2^23) with the sequential
 oracle, through the C ABI, and the same failure paths as the large-input
 kernel: Decoupled Fallback, timeout reporting, bounded look-back window,
 schedule perturbation.  Integers bit for bit; f32 within
@@ -19,9 +19,9 @@ if not torch.cuda.is_available():
 import device_wide_prefix_gb300 as dwp  # noqa: E402
 from device_wide_prefix_gb300 import build as dwp_build  # noqa: E402
 
-SMALL_MAX = 1 << 22
+SMALL_MAX = 1 << 23
 T = 3072        # elements per tile up to 2^18
-T2 = 15360      # elements per tile above 2^18, up to 2^22
+T2 = 15360      # elements per tile above 2^18, up to 2^23
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -60,7 +60,7 @@ def test_small_kernel_tiles_in_the_size_query():
     """One descriptor per 3072 elements up to 2^18; above, one per 15360
     elements but never fewer than at 2^18 (the size query does not shrink)."""
     for n, tiles in ((1, 1), (T, 1), (T + 1, 2), (1 << 18, 86), ((1 << 18) + 1, 86),
-                     (86 * T2 + 1, 87), (SMALL_MAX, 274)):
+                     (86 * T2 + 1, 87), (1 << 22, 274), (SMALL_MAX, 547)):
         assert dwp.scan_scratch_bytes(n) == 128 + 8 * tiles
 
 
