@@ -433,9 +433,6 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         if (t == kNoTile) break;
         uint32_t nkeep = 0, first = 0;  // this warp's kept records and its first output slot
         if (ld_volatile_smem(sm.lbres(i)) == 0u && *sm.tile_count(i) != 0u) {
-            uint32_t valid, fbulk;
-            tile_extent(t, valid, fbulk);
-            const uint64_t base = uint64_t(t) * TILE;
             uint4 *region = sm.recs(o) + cw * WR;
             const uint32_t *pre = sm.prefix(i);
             const uint32_t wfirst = pre[prefix_slot(cw * 32)] & 0xffffffu;

@@ -200,3 +200,46 @@ def test_two_level_size_query_and_validation(lib):
     assert R(0, 0, A + 4, A + 8192, n, s, need, 0)[0] == dwp.DWP_ERR_MISALIGNED
     assert R(0, 0, A, A + 16, n, s, need, 0)[0] == dwp.DWP_ERR_ALIASING
     assert R(0, 0, A, A + 8192, n, A + 32, need, 0)[0] == dwp.DWP_ERR_ALIASING
+
+
+def test_staged_compaction_size_query_and_validation(lib):
+    R = dwp.dwp_compact_by_flags_staged
+    scan = dwp.dwp_scan_exclusive
+    for n in (0, 1, 17, 1000, (1 << 23) + 1, 1 << 26):
+        st, need = R(0, 0, n, 0, 0, 0, 0, 0)
+        assert st == dwp.DWP_SUCCESS
+        scan_need = scan(dwp.DWP_U32_ADD, 0, 0, n, 0, 0, 0)[1]
+        r16 = lambda b: (b + 15) // 16 * 16  # noqa: E731
+        assert need == r16(scan_need) + 2 * r16(4 * n), n
+    n = 1000
+    _, need = R(0, 0, n, 0, 0, 0, 0, 0)
+    rec, fl, out, cnt, s = A, A + (1 << 20), A + (2 << 20), A + (3 << 20), A + (4 << 20)
+    assert R(rec, fl, n, out, cnt, s, need - 1, 0)[0] == dwp.DWP_ERR_SCRATCH_TOO_SMALL
+    assert R(rec, fl, n, out, 0, s, need, 0)[0] == dwp.DWP_ERR_INVALID_VALUE     # no count
+    assert R(0, fl, n, out, cnt, s, need, 0)[0] == dwp.DWP_ERR_INVALID_VALUE     # no records
+    assert R(rec + 8, fl, n, out, cnt, s, need, 0)[0] == dwp.DWP_ERR_MISALIGNED
+    assert R(rec, fl, n, out, cnt + 2, s, need, 0)[0] == dwp.DWP_ERR_MISALIGNED
+    assert R(rec, fl, n, rec + 16, cnt, s, need, 0)[0] == dwp.DWP_ERR_ALIASING  # out over records
+    assert R(rec, fl, n, out, out + 16, s, need, 0)[0] == dwp.DWP_ERR_ALIASING  # count inside out
+    assert R(rec, fl, n, out, cnt, fl, need, 0)[0] == dwp.DWP_ERR_ALIASING      # scratch over flags
+    assert R(rec, fl, 1 << 32, out, cnt, s, need, 0)[0] == dwp.DWP_ERR_INVALID_VALUE
+
+
+def test_test_hooks_validate_their_arguments(lib):
+    assert dwp.dwp_debug_set_delay(1, 1000001, 10) == dwp.DWP_ERR_INVALID_VALUE
+    assert dwp.dwp_debug_set_delay(1, 10, 100001) == dwp.DWP_ERR_INVALID_VALUE
+    assert dwp.dwp_debug_set_delay(0, 0, 0) == dwp.DWP_SUCCESS
+    assert dwp.dwp_debug_warp_scan_trace(A, 0, A, 0) == dwp.DWP_ERR_INVALID_VALUE
+    assert dwp.dwp_debug_warp_scan_trace(A, 33, A, 0) == dwp.DWP_ERR_INVALID_VALUE
+    assert dwp.dwp_debug_warp_scan_trace(0, 8, A, 0) == dwp.DWP_ERR_INVALID_VALUE
+    assert dwp.dwp_debug_warp_scan_trace(A, 8, 0, 0) == dwp.DWP_ERR_INVALID_VALUE
+    assert dwp.dwp_read_lookback_stats(0, 0)[0] == dwp.DWP_ERR_INVALID_VALUE
+    assert dwp.dwp_set_lookback_window(0) == dwp.DWP_SUCCESS
+
+
+def test_static_scratch_rejects_before_any_cuda_call(lib):
+    L = dwp.load()
+    assert L.dwp_scan_static_scratch(dwp.DWP_U32_ADD, 7, None, None, 10, None) == dwp.DWP_ERR_INVALID_VALUE
+    assert L.dwp_scan_static_scratch(9, dwp.DWP_EXCLUSIVE, None, None, 10, None) == dwp.DWP_ERR_INVALID_VALUE
+    assert (L.dwp_scan_static_scratch(dwp.DWP_U32_ADD, dwp.DWP_EXCLUSIVE, None, None, (1 << 28) + 1, None)
+            == dwp.DWP_ERR_SCRATCH_TOO_SMALL)
