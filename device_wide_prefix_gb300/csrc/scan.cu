@@ -78,7 +78,7 @@ struct ScanConfig {
     static_assert(RING_ >= SIN_ + SOUT_ + 2 + AHEAD_, "info ring shorter than the work in flight");
     static constexpr size_t kStageBytes = size_t(kTile) * 4;
     static constexpr int kPrefixWords = kConsumers + kConsumers / 8;
-    // info slot: 3 mbarriers + pad (32 B); tile id, aggregate, carry,
+    // info slot: 4 mbarriers (32 B); tile id, aggregate, carry,
     // look-back result (16 B); thread prefixes; 33 lane totals; 33 words of
     // look-back scratch
     static constexpr size_t kInfoBytes = 48 + 4 * kPrefixWords;
@@ -137,6 +137,8 @@ struct ScanSmem {
     __device__ uint64_t *info_ready(int i) const { return reinterpret_cast<uint64_t *>(info(i)); }
     __device__ uint64_t *carry_ready(int i) const { return info_ready(i) + 1; }
     __device__ uint64_t *info_free(int i) const { return info_ready(i) + 2; }
+    // the producer has written tile_id(i) (the tile is drawn)
+    __device__ uint64_t *id_ready(int i) const { return info_ready(i) + 3; }
     __device__ uint32_t *tile_id(int i) const { return reinterpret_cast<uint32_t *>(info(i) + 32); }
     __device__ uint32_t *agg(int i) const { return tile_id(i) + 1; }
     __device__ uint32_t *carry(int i) const { return tile_id(i) + 2; }
@@ -204,6 +206,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             mbar_init(sm.info_ready(i), 1);
             mbar_init(sm.carry_ready(i), 1);
             mbar_init(sm.info_free(i), NW);
+            mbar_init(sm.id_ready(i), 1);
         }
         *sm.abort_flag() = 0;
         *sm.end_iter() = kNoTile;
@@ -254,6 +257,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                     else perturb(fault, t, kSiteDraw);
                 }
                 *reinterpret_cast<volatile uint32_t *>(sm.tile_id(gi)) = t;
+                mbar_arrive(sm.id_ready(gi));  // the look-back may start now
                 ++taken;
                 if (t == kNoTile) {
                     // iteration g carries the sentinel down the pipeline;
@@ -411,11 +415,18 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 
     if (warp >= kLooker0 && warp < kReloader) {
         // --------------------------------------------------- look-back warps
+        // The look-back reads only predecessors' descriptors, so it starts
+        // as soon as the tile is drawn and runs while the tile loads and is
+        // reduced; the prefix goes out once the reducer has published the
+        // aggregate.  (With a bounded window an intermediate carries the
+        // tile's own aggregate, so there the look-back waits for the reduce
+        // first.)  Without the overlap the look-back's wait sat on every
+        // tile's path and cost 13% at 2^28.
         const uint32_t j = warp - kLooker0;
         bool draining = false;
         for (uint32_t k = j;; k += LW) {
             const int i = int(k % RING);
-            const int w = warp_wait_or_end(sm.info_ready(i), (k / RING) & 1u, k, sm.end_iter());
+            int w = warp_wait_or_end(sm.id_ready(i), (k / RING) & 1u, k, sm.end_iter());
             if (w != 2) {
                 if (w == 0 && lane == 0) record_error(hdr, DWP_ERR_PIPELINE_TIMEOUT);
                 return;
@@ -426,15 +437,30 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 return;
             }
             if (!draining && ld_volatile_smem(sm.abort_flag()) != 0) draining = true;
+            const bool early = fault.lookback_window == 0u;
             T carry = Op::identity();
-            int rc = (draining || ld_volatile_smem(sm.lbres(i)) != 0u) ? 1 : 0;
-            if (rc == 0) perturb(fault, t, kSiteLookback);
-            if (rc == 0 && t != 0)
+            int rc = draining ? 1 : 0;
+            if (early && rc == 0 && t != 0) {
+                perturb(fault, t, kSiteLookback);
+                rc = lookback<Op, C::kLookK>(desc, t, lane, fault.spin_limit, fault.fallback_polls,
+                                             ScanRescue<Op, TILE>{in, n}, hdr, 0u, 0u, false,
+                                             sm.lb_scratch(int(j)), &carry);
+            }
+            // the tile's aggregate (or the reducer's verdict on it)
+            w = warp_wait_or_end(sm.info_ready(i), (k / RING) & 1u, k, sm.end_iter());
+            if (w != 2) {
+                if (w == 0 && lane == 0) record_error(hdr, DWP_ERR_PIPELINE_TIMEOUT);
+                return;
+            }
+            if (ld_volatile_smem(sm.lbres(i)) != 0u) rc = 1;  // the reducer gave the tile up
+            if (!early && rc == 0 && t != 0) {
+                perturb(fault, t, kSiteLookback);
                 rc = lookback<Op, C::kLookK>(desc, t, lane, fault.spin_limit, fault.fallback_polls,
                                              ScanRescue<Op, TILE>{in, n}, hdr,
                                              fault.lookback_window, *sm.agg(i),
                                              t != fault.never_publish_tile, sm.lb_scratch(int(j)),
                                              &carry);
+            }
             if (rc == 0) perturb(fault, t, kSitePrefix);
             if (lane == 0) {
                 if (rc == 0) {
