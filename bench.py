@@ -162,6 +162,24 @@ class ClockSampler:
                 "window": "timed region" if inside else "last samples (timed region shorter than the sampling period)"}
 
 
+def max_over_ranks(dist, v: float, device) -> float:
+    """The largest of every rank's v (a time), through one all-reduce on
+    `device` (the GPU under NCCL; the CPU under gloo).  With dist None (one
+    process) v itself."""
+    if dist is None:
+        return v
+    import torch
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_value(units_per_rank: int, world: int, ms_max: float) -> float:
+    """Whole-job throughput of `world` replicas, each processing
+    units_per_rank, timed by the slowest rank: units per second / 1e9."""
+    return world * units_per_rank / (ms_max * 1e-3) / 1e9
+
+
 def host_cores() -> dict:
     """Host CPU cores: all of them, and those this process may run on."""
     try:
@@ -259,12 +277,8 @@ def main() -> None:
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    def max_over_ranks(v: float) -> float:
-        if dist is None:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    def ranks_max(v: float) -> float:
+        return max_over_ranks(dist, v, dev)
 
     import ctypes
     n = 1 << args.log2n
@@ -306,8 +320,8 @@ def main() -> None:
     st = dwp.read_status(scratch)
     if st != dwp.DWP_SUCCESS:
         raise RuntimeError("device status after timed steps: %s" % dwp.status_string(st))
-    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps)
-    value = world * n / (ms * 1e-3) / 1e9
+    ms = ranks_max(e0.elapsed_time(e1) / args.steps)
+    value = replica_value(n, world, ms)
 
     # end to end from pinned host memory through the same C entry point:
     # every step copies its input in, scans it and copies the result out.
@@ -326,7 +340,7 @@ def main() -> None:
         y_host[0].copy_(y, non_blocking=True)
     e1.record(stream)
     barrier()
-    e2e_serial_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps)
+    e2e_serial_ms = ranks_max(e0.elapsed_time(e1) / e2e_steps)
     sides = [torch.cuda.Stream(dev) for _ in range(2)]
     xs, ys, scr2 = [x, torch.empty_like(x)], [y, torch.empty_like(y)], [scratch, dwp.alloc_scratch(need, dev)]
 
@@ -353,7 +367,7 @@ def main() -> None:
         stream.wait_stream(s)
     e1.record(stream)
     barrier()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps)
+    e2e_ms = ranks_max(e0.elapsed_time(e1) / e2e_steps)
     for j in range(2):
         if dwp.read_status(scr2[j]) != dwp.DWP_SUCCESS:
             raise RuntimeError("device status after the end-to-end steps")
