@@ -47,6 +47,7 @@ constexpr int kSmallWarps = kSmallThreads / 32;
 // at about the same time, so most look-backs fold aggregates back to tile 0
 // rather than stop at a recent prefix: a poll covers 32 K predecessors.
 __host__ __device__ constexpr int small_look_k(int items) { return items <= 12 ? 4 : 8; }
+static_assert(kSmallThreads == 256, "tile sizes below assume 256 threads");
 
 // Dynamic shared memory: the tile stage, then the mbarrier.
 template <int ITEMS>
@@ -190,7 +191,8 @@ __global__ void __launch_bounds__(kSmallThreads, 2)
     __syncthreads();
     if (s_rc != 0u) return;  // the output of an abandoned tile is not written
 
-    // -- scan the registers from carry + prefix into the stage; one bulk store
+    // -- scan the registers from carry + prefix into the stage; one bulk
+    //    store (per-warp stores measured no faster)
     T run = Op::combine(Op::combine(Op::from_bits(s_carry), wpre), excl_in_warp);
     uint4 *dv = reinterpret_cast<uint4 *>(stage + p0);
 #pragma unroll
@@ -239,25 +241,42 @@ cudaError_t launch_small_items(const void *in, void *out, uint64_t n, void *scra
                       reinterpret_cast<typename Op::T *>(out), n, uint32_t(tiles), hdr, desc, fault);
 }
 
-// Up to 2^18 elements a tile is 256 * 12 = 3072 elements (at most 86
-// tiles); above, 256 * 60 = 15360 (at most 547 tiles up to 2^23).
-constexpr uint64_t kSmallSplit = uint64_t(1) << 18;
+// Tile sizes grow with n in three tiers, so the number of tiles polling the
+// descriptors at once stays low: 256 * 12 = 3072 elements up to 2^18 (at
+// most 86 tiles), 256 * 28 = 7168 up to 2^20 (at most 147), 256 * 60 = 15360
+// above (at most 547 up to 2^23).
+#ifndef DWP_SMALL_TIER1_LOG2
+#define DWP_SMALL_TIER1_LOG2 18
+#endif
+#ifndef DWP_SMALL_TIER2_LOG2
+#define DWP_SMALL_TIER2_LOG2 20
+#endif
+constexpr uint64_t kSmallTier1 = uint64_t(1) << DWP_SMALL_TIER1_LOG2;
+constexpr uint64_t kSmallTier2 = uint64_t(1) << DWP_SMALL_TIER2_LOG2;
 
 template <class Op, bool INCL>
 cudaError_t launch_small(const void *in, void *out, uint64_t n, void *scratch, cudaStream_t stream,
                          const LaunchKnobs &fault) {
-    return n <= kSmallSplit ? launch_small_items<Op, INCL, 12>(in, out, n, scratch, stream, fault)
-                            : launch_small_items<Op, INCL, 60>(in, out, n, scratch, stream, fault);
+    if (n <= kSmallTier1) return launch_small_items<Op, INCL, 12>(in, out, n, scratch, stream, fault);
+    if (n <= kSmallTier2) return launch_small_items<Op, INCL, 28>(in, out, n, scratch, stream, fault);
+    return launch_small_items<Op, INCL, 60>(in, out, n, scratch, stream, fault);
 }
 
 }  // namespace
 
 uint64_t scan_small_descriptors(uint64_t n) {
-    constexpr uint64_t t12 = SmallSmem<12>::kTile, t60 = SmallSmem<60>::kTile;
-    if (n <= kSmallSplit) return (n + t12 - 1) / t12;
-    const uint64_t at_split = (kSmallSplit + t12 - 1) / t12;  // 86
-    const uint64_t tiles = (n + t60 - 1) / t60;
-    return tiles > at_split ? tiles : at_split;
+    // at least the tile count, and never fewer than the largest count of a
+    // lower tier, so the size query does not shrink as n grows
+    constexpr uint64_t t1 = SmallSmem<12>::kTile, t2 = SmallSmem<28>::kTile, t3 = SmallSmem<60>::kTile;
+    constexpr uint64_t max1 = (kSmallTier1 + t1 - 1) / t1;
+    constexpr uint64_t max2 = (kSmallTier2 + t2 - 1) / t2 > max1 ? (kSmallTier2 + t2 - 1) / t2 : max1;
+    if (n <= kSmallTier1) return (n + t1 - 1) / t1;
+    if (n <= kSmallTier2) {
+        const uint64_t tiles = (n + t2 - 1) / t2;
+        return tiles > max1 ? tiles : max1;
+    }
+    const uint64_t tiles = (n + t3 - 1) / t3;
+    return tiles > max2 ? tiles : max2;
 }
 
 cudaError_t launch_scan_small(dwp_op op, bool inclusive, const void *in, void *out, uint64_t n,

@@ -1,5 +1,5 @@
 """Parity of the small-input plain scan (one block per tile of 3072 elements
-up to n = 2^18, of 15360 elements up to n = 2^23) with the sequential
+up to n = 2^18, 7168 up to 2^20, 15360 up to n = 2^23) with the sequential
 oracle, through the C ABI, and the same failure paths as the large-input
 kernel: Decoupled Fallback, timeout reporting, bounded look-back window,
 schedule perturbation.  Integers bit for bit; f32 within
@@ -21,7 +21,18 @@ from device_wide_prefix_gb300 import build as dwp_build  # noqa: E402
 
 SMALL_MAX = 1 << 23
 T = 3072        # elements per tile up to 2^18
-T2 = 15360      # elements per tile above 2^18, up to 2^23
+TM = 7168       # elements per tile above 2^18, up to 2^20
+T2 = 15360      # elements per tile above 2^20, up to 2^23
+
+
+def descriptors(n):
+    """The size query's descriptor count: the tile count, never fewer than
+    the largest count of a lower tier."""
+    if n <= 1 << 18:
+        return -(-n // T)
+    if n <= 1 << 20:
+        return max(-(-n // TM), 86)
+    return max(-(-n // T2), 147)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -57,32 +68,35 @@ def check(ref, x, op, inclusive, y):
 
 
 def test_small_kernel_tiles_in_the_size_query():
-    """One descriptor per 3072 elements up to 2^18; above, one per 15360
-    elements but never fewer than at 2^18 (the size query does not shrink)."""
+    """One descriptor per tile of the tier n falls in, never fewer than the
+    largest count of a lower tier (the size query does not shrink)."""
     for n, tiles in ((1, 1), (T, 1), (T + 1, 2), (1 << 18, 86), ((1 << 18) + 1, 86),
-                     (86 * T2 + 1, 87), (1 << 22, 274), (SMALL_MAX, 547)):
-        assert dwp.scan_scratch_bytes(n) == 128 + 8 * tiles
+                     (87 * TM, 87), (1 << 20, 147), ((1 << 20) + 1, 147), (148 * T2, 148),
+                     (1 << 22, 274), (SMALL_MAX, 547)):
+        assert descriptors(n) == tiles, n
+        assert dwp.scan_scratch_bytes(n) == 128 + 8 * tiles, n
 
 
 @pytest.mark.parametrize("op", ["u32_add", "u32_max", "f32_add"])
 @pytest.mark.parametrize("inclusive", [False, True])
 def test_sizes_around_tiles_and_the_switch(ref, op, inclusive):
     for n in (1, 3, 15, 16, 17, T - 1, T, T + 1, 3 * T + 5, 100003, 1 << 18, (1 << 18) + 1,
-              T2 * 7 - 1, T2 * 7 + 3, SMALL_MAX - 1, SMALL_MAX, SMALL_MAX + 1):
+              TM * 50 - 1, TM * 50 + 3, (1 << 20) + 1, T2 * 70 - 1, T2 * 70 + 3, SMALL_MAX - 1,
+              SMALL_MAX, SMALL_MAX + 1):
         x = values(n, op, 700 + n % 97)
         y, scratch = run(x, op, inclusive)
         assert dwp.read_status(scratch) == dwp.DWP_SUCCESS
         check(ref, x, op, inclusive, y)
 
 
-@pytest.mark.parametrize("n", [50 * T + 9, 200 * T2 + 9])
+@pytest.mark.parametrize("n", [50 * T + 9, 100 * TM + 9, 200 * T2 + 9])
 def test_in_place(ref, n):
     x = values(n, "u32_add", 5)
     y, _ = run(x.copy(), "u32_add", False, inplace=True)
     check(ref, x, "u32_add", False, y)
 
 
-@pytest.mark.parametrize("tile,tiles", [(T, 60), (T2, 250)])
+@pytest.mark.parametrize("tile,tiles", [(T, 60), (TM, 120), (T2, 250)])
 @pytest.mark.parametrize("silent", ["first", "inner", "last"])
 @pytest.mark.parametrize("op,inclusive", [("u32_add", False), ("f32_add", True)])
 def test_fallback_rescues_a_silent_tile(ref, tile, tiles, silent, op, inclusive):
@@ -102,7 +116,7 @@ def test_fallback_rescues_a_silent_tile(ref, tile, tiles, silent, op, inclusive)
     check(ref, x, op, inclusive, y)
 
 
-@pytest.mark.parametrize("n", [60 * T, 250 * T2])
+@pytest.mark.parametrize("n", [60 * T, 120 * TM, 250 * T2])
 def test_timeout_is_reported_not_hung(ref, n):
     x = values(n, "u32_add", 32)
     try:
@@ -133,7 +147,7 @@ def test_bounded_window(ref, window):
 
 
 @pytest.mark.parametrize("seed", [0x61, 0x62])
-@pytest.mark.parametrize("n", [(1 << 18) - 5, SMALL_MAX - 1234])
+@pytest.mark.parametrize("n", [(1 << 18) - 5, (1 << 20) - 77, SMALL_MAX - 1234])
 @pytest.mark.parametrize("op,inclusive", [("u32_add", False), ("u32_max", True), ("f32_add", True)])
 def test_under_perturbation(ref, seed, n, op, inclusive):
     x = values(n, op, seed)
