@@ -59,10 +59,8 @@ struct CompactConfig {
     static constexpr size_t kFlagBytes = (size_t(kTile) + 15) / 16 * 16;
     static constexpr int kPrefixWords = kConsumers + kConsumers / 8;
     // info slot: 3 mbarriers + pad (32 B); tile id, carry, look-back result,
-    // tile count (16 B); flags; thread prefixes; lane totals 33; look-back
-    // scratch 33 (+ pad to 16 B)
-    static constexpr size_t kInfoBytes =
-        (48 + kFlagBytes + 4 * (kPrefixWords + 33 + 33) + 15) / 16 * 16;
+    // tile count (16 B); flags; thread prefixes; lane totals 33 (+ pad to 16 B)
+    static constexpr size_t kInfoBytes = (48 + kFlagBytes + 4 * (kPrefixWords + 33) + 15) / 16 * 16;
     static constexpr size_t kBarBytes = 16 * SOUT_;
     static constexpr size_t kSmemBytes = kRecBytes * SOUT_ + kInfoBytes * RING_ + kBarBytes + 16;
 };
@@ -117,7 +115,6 @@ struct CmpSmem {
         return reinterpret_cast<uint32_t *>(flags(i) + C::kFlagBytes);
     }
     __device__ uint32_t *lane_tot(int i) const { return prefix(i) + C::kPrefixWords; }
-    __device__ uint32_t *lb_scratch(int i) const { return lane_tot(i) + 33; }
     __device__ uint64_t *bars() const {
         return reinterpret_cast<uint64_t *>(base + C::kRecBytes * C::kOut + C::kInfoBytes * C::kRing);
     }
@@ -153,7 +150,7 @@ struct CompactRescue {
     static_assert(TILE % 16 == 0, "full tiles are read as 16-byte vectors");
     const uint8_t *flags;
     uint64_t n;
-    __device__ uint64_t operator()(uint32_t p, uint32_t lane, uint32_t *) const {
+    __device__ uint64_t operator()(uint32_t p, uint32_t lane) const {
         const uint64_t b = uint64_t(p) * TILE;
         const uint64_t e = min(n, b + uint64_t(TILE));
         uint32_t cnt = 0;
@@ -358,7 +355,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 rc = lookback<Op, C::kLookK>(desc, t, lane, fault.spin_limit, fault.fallback_polls,
                                              CompactRescue<TILE>{flags, n}, hdr,
                                              fault.lookback_window, total,
-                                             t != fault.never_publish_tile, sm.lb_scratch(i), &carry);
+                                             t != fault.never_publish_tile, &carry);
             if (rc == 0) perturb(fault, t, kSitePrefix);
             if (DWP_CMP_PREFETCH == 3 && lane == 0 && rc == 0 && total != 0u)
                 bulk_prefetch_l2(recs + base, valid * 16u, l2_policy_evict_last());

@@ -26,10 +26,8 @@ struct OpU32Add {
     static __device__ __forceinline__ T combine(T a, T b) { return a + b; }
     static __device__ __forceinline__ uint32_t to_bits(T v) { return v; }
     static __device__ __forceinline__ T from_bits(uint32_t b) { return b; }
-    // one redux instruction; `scratch` unused
-    static __device__ __forceinline__ T warp_reduce(T v, uint32_t, uint32_t *) {
-        return __reduce_add_sync(0xffffffffu, v);
-    }
+    // one redux instruction
+    static __device__ __forceinline__ T warp_reduce(T v) { return __reduce_add_sync(0xffffffffu, v); }
 };
 
 struct OpU32Max {
@@ -39,9 +37,7 @@ struct OpU32Max {
     static __device__ __forceinline__ T combine(T a, T b) { return a > b ? a : b; }
     static __device__ __forceinline__ uint32_t to_bits(T v) { return v; }
     static __device__ __forceinline__ T from_bits(uint32_t b) { return b; }
-    static __device__ __forceinline__ T warp_reduce(T v, uint32_t, uint32_t *) {
-        return __reduce_max_sync(0xffffffffu, v);
-    }
+    static __device__ __forceinline__ T warp_reduce(T v) { return __reduce_max_sync(0xffffffffu, v); }
 };
 
 struct OpF32Add {
@@ -51,21 +47,15 @@ struct OpF32Add {
     static __device__ __forceinline__ T combine(T a, T b) { return __fadd_rn(a, b); }
     static __device__ __forceinline__ uint32_t to_bits(T v) { return __float_as_uint(v); }
     static __device__ __forceinline__ T from_bits(uint32_t b) { return __uint_as_float(b); }
-    // No float redux instruction: one lane adds the 32 values through a
-    // 33-word shared-memory scratch owned by the calling warp.
-    static __device__ __forceinline__ T warp_reduce(T v, uint32_t lane, uint32_t *scratch) {
-        scratch[lane] = __float_as_uint(v);
-        __syncwarp();
-        if (lane == 0) {
-            float acc = 0.0f;
+    // No float redux instruction: a shuffle butterfly (xor 16, 8, 4, 2, 1),
+    // then lane 0's sum goes to every lane, so all lanes return the same
+    // bits.  The look-back's warp reduction lies on the path by which the
+    // prefix frontier advances; the butterfly replaced a sum by one lane
+    // through shared memory that cost 6% of a 2^28 scan.
+    static __device__ __forceinline__ T warp_reduce(T v) {
 #pragma unroll
-            for (int l = 0; l < 32; ++l) acc = __fadd_rn(acc, __uint_as_float(scratch[l]));
-            scratch[32] = __float_as_uint(acc);
-        }
-        __syncwarp();
-        const float r = __uint_as_float(scratch[32]);
-        __syncwarp();
-        return r;
+        for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+        return __shfl_sync(0xffffffffu, v, 0);
     }
 };
 
@@ -374,12 +364,14 @@ __device__ __forceinline__ uint32_t warp_lower_bound(const uint32_t *off, uint32
 // lane first and then across lanes; for f32 only the grouping changes, the
 // run-to-run variation the method has anyway ("When not to use it").
 // Warp collectives are kept to a few per poll: on a GB300 streaming at full
-// bandwidth each one was measured at several hundred cycles.
+// bandwidth a dependent one was measured at several hundred cycles in the
+// reducer.  The f32 sum of a window is still a shuffle butterfly: there a
+// one-lane sum through shared memory measured slower (6% of a 2^28 scan).
 //
 // Decoupled Fallback ("GPU Prefix Sums", section "Decoupled Fallback"): with
 // fallback_polls > 0, once a window has been polled fallback_polls times with
 // a predecessor still unpublished, the warp stops waiting for it.  For each
-// such predecessor p, `rescue(p, lane, scratch)` (called by all 32 lanes,
+// such predecessor p, `rescue(p, lane)` (called by all 32 lanes,
 // same result on each) reduces tile p straight from the input and returns
 // the descriptor p would publish; lane 0 installs it with a compare-and-swap
 // against the invalid state.  So of several rescuers and the tile's own
@@ -409,7 +401,7 @@ __device__ __forceinline__ int lookback(uint64_t *desc, uint32_t t, uint32_t lan
                                         uint32_t spin_limit, uint32_t fallback_polls,
                                         const Rescue &rescue, ScratchHeader *hdr,
                                         uint32_t window, uint32_t own, bool publish,
-                                        uint32_t *scratch, typename Op::T *carry_out) {
+                                        typename Op::T *carry_out) {
     using T = typename Op::T;
     static_assert(Op::kCommutative, "the look-back combines per lane first");
     static_assert(K * 32 < (1 << 29), "window positions must fit the key");
@@ -455,7 +447,7 @@ __device__ __forceinline__ int lookback(uint64_t *desc, uint32_t t, uint32_t lan
                         const uint32_t j = uint32_t(__ffs(need)) - 1u;
                         need &= need - 1u;
                         const uint32_t p = static_cast<uint32_t>(base - 32 * i - static_cast<int64_t>(j));
-                        const uint64_t mine = rescue(p, lane, scratch);
+                        const uint64_t mine = rescue(p, lane);
                         unsigned long long got = 0ull;
                         if (lane == 0) {
                             const unsigned long long old = atomicCAS(
@@ -488,7 +480,7 @@ __device__ __forceinline__ int lookback(uint64_t *desc, uint32_t t, uint32_t lan
             if (32u * i + lane <= last) acc = Op::combine(acc, Op::from_bits(desc_bits(d[i])));
             if (32u * i + lane == last && kind == 2u) span = desc_state(d[i]) - kSpan0;
         }
-        carry = Op::combine(Op::warp_reduce(acc, lane, scratch), carry);
+        carry = Op::combine(Op::warp_reduce(acc), carry);
         if (kind == 0u) break;
         if (kind == 2u && lane == 0) atomicAdd(&hdr->jumps, 1u);
         // the intermediate at position `last` covers `span` tiles ending at it
@@ -516,7 +508,7 @@ struct ScanRescue {
     static_assert(TILE % 4 == 0, "full tiles are read as 16-byte vectors");
     const typename Op::T *in;
     uint64_t n;
-    __device__ uint64_t operator()(uint32_t p, uint32_t lane, uint32_t *scratch) const {
+    __device__ uint64_t operator()(uint32_t p, uint32_t lane) const {
         using T = typename Op::T;
         const uint64_t b = uint64_t(p) * TILE;
         const uint64_t e = min(n, b + uint64_t(TILE));
@@ -531,7 +523,7 @@ struct ScanRescue {
         } else {
             for (uint64_t q = b + lane; q < e; q += 32u) acc = Op::combine(acc, in[q]);
         }
-        const T tot = Op::warp_reduce(acc, lane, scratch);
+        const T tot = Op::warp_reduce(acc);
         return make_desc(p == 0 ? kPrefix : kAggregate, Op::to_bits(tot));
     }
 };

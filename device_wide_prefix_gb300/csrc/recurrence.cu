@@ -70,9 +70,8 @@ struct RecConfig {
     // tile A, tile B, pad x3 (32 B); thread prefix maps, A then B
     static constexpr size_t kInfoBytes = 64 + 8 * size_t(kPrefixWords);
     static constexpr size_t kBarBytes = 16 * (SIN_ + SOUT_);
-    // per-warp scratch after the barriers: 66 words per reducer and per
-    // look-back warp (32 A, 32 B, a result pair)
-    static constexpr size_t kWarpScratchBytes = 4 * 66 * size_t(SIN_ + LW_);
+    // per-reducer scratch after the barriers: its 32 lane maps (32 A, 32 B)
+    static constexpr size_t kWarpScratchBytes = 4 * 64 * size_t(SIN_);
     static constexpr size_t kSmemBytes =
         kStageBytes * (SIN_ + SOUT_) + kInfoBytes * RING_ + kBarBytes + 16 + kWarpScratchBytes;
     static_assert(kThreads <= 1024, "more than 1024 threads per block");
@@ -140,9 +139,9 @@ struct RecSmem {
         return reinterpret_cast<uint32_t *>(bars() + 2 * (C::kIn + C::kOut));
     }
     __device__ uint32_t *end_iter() const { return abort_flag() + 1; }
-    // reducer r's and look-back warp j's 66-word scratch
+    // reducer r's 64-word scratch
     __device__ float *warp_scratch(int w) const {
-        return reinterpret_cast<float *>(abort_flag() + 4) + 66 * w;
+        return reinterpret_cast<float *>(abort_flag() + 4) + 64 * w;
     }
 };
 
@@ -164,30 +163,31 @@ __device__ __forceinline__ void rec_elem(const float *sa, const float *sb, const
     }
 }
 
-// Fold 32 maps, one per lane, into their composition through `s` (66
-// words): each lane stores its map at position `slot` (a permutation of
-// 0..31), and position 0 is applied first.  All lanes get the result.  One
-// lane composes serially: no warp shuffles on this path.
-__device__ __forceinline__ void warp_compose(float a, float b, uint32_t slot, float *s, float &ra,
-                                             float &rb) {
-    const uint32_t lane = threadIdx.x & 31u;
-    s[slot] = a;
-    s[32 + slot] = b;
-    __syncwarp();
-    if (lane == 0) {
-        float A = 1.0f, B = 0.0f;
+// Fold 32 maps x -> a x + b, one per lane, into their composition by a
+// shuffle tree; every lane gets the result.  LANE0_FIRST: lane 0's map is
+// applied first and lane 31's last; otherwise the reverse.  After the step
+// of width o, lane l holds the composite of lanes l .. l+o-1.  The map is
+// not commutative, so each step composes the two halves in their order.
+// (The look-back's fold lies on the path by which the prefix frontier
+// advances; this tree replaced a serial fold by one lane through shared
+// memory.)
+template <bool LANE0_FIRST>
+__device__ __forceinline__ void warp_compose(float a, float b, uint32_t lane, float &ra, float &rb) {
 #pragma unroll
-        for (int l = 0; l < 32; ++l) {
-            B = __fmaf_rn(s[l], B, s[32 + l]);
-            A = __fmul_rn(s[l], A);
+    for (uint32_t o = 1; o < 32u; o <<= 1) {
+        const float a2 = __shfl_down_sync(0xffffffffu, a, o);
+        const float b2 = __shfl_down_sync(0xffffffffu, b, o);
+        if (lane + o < 32u) {
+            if (LANE0_FIRST) {
+                b = __fmaf_rn(a2, b, b2);  // (a, b) first, then (a2, b2)
+            } else {
+                b = __fmaf_rn(a, b2, b);   // (a2, b2) first, then (a, b)
+            }
+            a = __fmul_rn(a2, a);
         }
-        s[64] = A;
-        s[65] = B;
     }
-    __syncwarp();
-    ra = s[64];
-    rb = s[65];
-    __syncwarp();
+    ra = __shfl_sync(0xffffffffu, a, 0);
+    rb = __shfl_sync(0xffffffffu, b, 0);
 }
 
 // Decoupled Fallback for the recurrence: the two descriptor words tile p
@@ -199,7 +199,7 @@ struct RecRescue {
     const float *b;
     uint64_t n;
     uint32_t tile;
-    __device__ void operator()(uint32_t p, uint32_t lane, float *s, uint64_t &w0,
+    __device__ void operator()(uint32_t p, uint32_t lane, uint64_t &w0,
                                uint64_t &w1) const {
         const uint64_t t0 = uint64_t(p) * tile;
         const uint64_t e = min(n, t0 + uint64_t(tile));
@@ -213,7 +213,7 @@ struct RecRescue {
             A = __fmul_rn(aq, A);
         }
         float TA, TB;
-        warp_compose(A, B, lane, s, TA, TB);
+        warp_compose<true>(A, B, lane, TA, TB);
         if (p == 0) {
             w0 = 0ull;
             w1 = make_desc(kPrefix, __float_as_uint(TB));
@@ -239,7 +239,7 @@ struct RecRescue {
 __device__ __forceinline__ int lookback_affine(uint64_t *desc, uint32_t t, uint32_t lane,
                                                uint32_t spin_limit, uint32_t fallback_polls,
                                                const RecRescue &rescue, uint32_t *fallbacks,
-                                               float *s, float *carry_out) {
+                                               float *carry_out) {
     float accA = 1.0f, accB = 0.0f;  // composition of the nearer windows, applied last
     int64_t base = static_cast<int64_t>(t) - 1;
     uint32_t polls = 0;
@@ -269,7 +269,7 @@ __device__ __forceinline__ int lookback_affine(uint64_t *desc, uint32_t t, uint3
                     need &= need - 1u;
                     const uint32_t p = static_cast<uint32_t>(base - static_cast<int64_t>(j));
                     uint64_t m0, m1;
-                    rescue(p, lane, s, m0, m1);
+                    rescue(p, lane, m0, m1);
                     unsigned long long g0 = 0ull, g1 = 0ull;
                     if (lane == 0) {
                         auto *d0 = reinterpret_cast<unsigned long long *>(desc + 2 * uint64_t(p));
@@ -306,10 +306,10 @@ __device__ __forceinline__ int lookback_affine(uint64_t *desc, uint32_t t, uint3
             ma = 0.0f;
             mb = __uint_as_float(desc_bits(w1));
         }
-        // lane 0 is the nearest tile and is applied last: lane l takes
-        // position 31 - l, so the farthest tile comes first
+        // lane 0 is the nearest tile and is applied last, the farthest
+        // (lane 31) first
         float WA, WB;
-        warp_compose(ma, mb, 31u - lane, s, WA, WB);
+        warp_compose<false>(ma, mb, lane, WA, WB);
         // total = (nearer windows) after (this window)
         accB = __fmaf_rn(accA, WB, accB);
         accA = __fmul_rn(accA, WA);
@@ -565,7 +565,6 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     if (warp >= kLooker0 && warp < kReloader) {
         // --------------------------------------------------- look-back warps
         const uint32_t j = warp - kLooker0;
-        float *scr = sm.warp_scratch(SIN + int(j));
         const RecRescue rescue{ga, gb, n, uint32_t(TILE)};
         bool draining = false;
         for (uint32_t k = j;; k += LW) {
@@ -586,7 +585,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             if (PERTURB && rc == 0) perturb(fault, t, kSiteLookback);
             if (rc == 0 && t != 0)
                 rc = lookback_affine(desc, t, lane, fault.spin_limit, fault.fallback_polls, rescue,
-                                     &hdr->fallbacks, scr, &carry);
+                                     &hdr->fallbacks, &carry);
             if (PERTURB && rc == 0) perturb(fault, t, kSitePrefix);
             if (lane == 0) {
                 if (rc == 0) {

@@ -79,12 +79,10 @@ struct ScanConfig {
     static constexpr size_t kStageBytes = size_t(kTile) * 4;
     static constexpr int kPrefixWords = kConsumers + kConsumers / 8;
     // info slot: 4 mbarriers (32 B); tile id, aggregate, carry,
-    // look-back result (16 B); thread prefixes; 33 lane totals; 33 words of
-    // look-back scratch
+    // look-back result (16 B); thread prefixes
     static constexpr size_t kInfoBytes = 48 + 4 * kPrefixWords;
-    // per-warp scratch after the barriers: 33 lane totals per reducer, 33
-    // words per look-back warp (f32 warp reduction)
-    static constexpr size_t kWarpScratchBytes = 4 * 33 * (SIN_ + LW_);
+    // per-reducer scratch after the barriers: 33 lane totals
+    static constexpr size_t kWarpScratchBytes = 4 * 33 * SIN_;
     // stage barriers: per input stage full + empty, per output stage ready + empty
     static constexpr size_t kBarBytes = 16 * (SIN_ + SOUT_);
     static constexpr size_t kSmemBytes =
@@ -158,9 +156,8 @@ struct ScanSmem {
     }
     // first ring iteration that holds no tile (set once by the producer)
     __device__ uint32_t *end_iter() const { return abort_flag() + 1; }
-    // reducer r's 33 lane totals; look-back warp j's 33-word scratch
+    // reducer r's 33 lane totals
     __device__ uint32_t *lane_tot(int r) const { return abort_flag() + 4 + 33 * r; }
-    __device__ uint32_t *lb_scratch(int j) const { return abort_flag() + 4 + 33 * (C::kIn + j); }
 };
 
 // Elements pos .. pos+3 of a tile as one vector when they lie past the
@@ -443,8 +440,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             if (early && rc == 0 && t != 0) {
                 perturb(fault, t, kSiteLookback);
                 rc = lookback<Op, C::kLookK>(desc, t, lane, fault.spin_limit, fault.fallback_polls,
-                                             ScanRescue<Op, TILE>{in, n}, hdr, 0u, 0u, false,
-                                             sm.lb_scratch(int(j)), &carry);
+                                             ScanRescue<Op, TILE>{in, n}, hdr, 0u, 0u, false, &carry);
             }
             // the tile's aggregate (or the reducer's verdict on it)
             w = warp_wait_or_end(sm.info_ready(i), (k / RING) & 1u, k, sm.end_iter());
@@ -458,8 +454,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 rc = lookback<Op, C::kLookK>(desc, t, lane, fault.spin_limit, fault.fallback_polls,
                                              ScanRescue<Op, TILE>{in, n}, hdr,
                                              fault.lookback_window, *sm.agg(i),
-                                             t != fault.never_publish_tile, sm.lb_scratch(int(j)),
-                                             &carry);
+                                             t != fault.never_publish_tile, &carry);
             }
             if (rc == 0) perturb(fault, t, kSitePrefix);
             if (lane == 0) {

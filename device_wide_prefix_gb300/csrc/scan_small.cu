@@ -69,7 +69,6 @@ __global__ void __launch_bounds__(kSmallThreads, 2)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem_raw + SmallSmem<ITEMS>::kStageBytes);
     __shared__ uint32_t s_tile, s_ok, s_carry, s_rc;
     __shared__ uint32_t s_wtot[kSmallWarps];
-    __shared__ uint32_t s_lb[33];  // look-back scratch (f32 warp reduction)
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
     if (threadIdx.x == 0) {
         mbar_init(full, 1);
@@ -173,7 +172,7 @@ __global__ void __launch_bounds__(kSmallThreads, 2)
                                                    fault.fallback_polls,
                                                    ScanRescue<Op, int(TILE)>{in, n}, hdr,
                                                    fault.lookback_window, Op::to_bits(agg),
-                                                   t != fault.never_publish_tile, s_lb, &carry);
+                                                   t != fault.never_publish_tile, &carry);
         if (rc == 0) perturb(fault, t, kSitePrefix);
         if (lane == 0) {
             if (rc == 0) {

@@ -68,9 +68,9 @@ struct SegConfig {
     // info slot: 3 mbarriers + pad (32 B); tile id, aggregate, carry,
     // look-back result, aggregate head, first-row head, pad x2 (32 B);
     // prefix values; prefix head bytes; head bitmap; lane totals 33; lane
-    // heads 33; look-back scratch 33
+    // heads 33 (+ pad to 16 B)
     static constexpr size_t kInfoBytes =
-        64 + 4 * (kPrefixWords + kPHeadWords + kHeadWords + 33 + 33 + 33);
+        (64 + 4 * (kPrefixWords + kPHeadWords + kHeadWords + 33 + 33) + 15) / 16 * 16;
     static_assert(kInfoBytes % 8 == 0, "info slots hold mbarriers");
     static constexpr size_t kBarBytes = 16 * (SIN_ + SOUT_) + 8 * SIN_;
     // + abort, end, cover lo, cover hi, then the offset sample
@@ -139,7 +139,6 @@ struct SegSmem {
     __device__ uint32_t *heads(int i) const { return prefix(i) + C::kPrefixWords + C::kPHeadWords; }
     __device__ uint32_t *lane_tot(int i) const { return heads(i) + C::kHeadWords; }
     __device__ uint32_t *lane_head(int i) const { return lane_tot(i) + 33; }
-    __device__ uint32_t *lb_scratch(int i) const { return lane_head(i) + 33; }
     __device__ uint64_t *bars() const {
         return reinterpret_cast<uint64_t *>(base + C::kStageBytes * (C::kIn + C::kOut) +
                                             C::kInfoBytes * C::kRing);
@@ -188,7 +187,7 @@ struct SegRescue {
     uint32_t nseg;
     uint64_t n;
     uint32_t tile;
-    __device__ uint64_t operator()(uint32_t p, uint32_t lane, uint32_t *) const {
+    __device__ uint64_t operator()(uint32_t p, uint32_t lane) const {
         const uint64_t b = uint64_t(p) * tile;
         const uint64_t e = min(n, b + uint64_t(tile));  // e <= n < 2^32
         const uint32_t k = warp_lower_bound(off, 0u, nseg + 1u, uint32_t(e), lane);
@@ -555,8 +554,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 rc = lookback<Op, C::kLookK>(desc, t, lane, fault.spin_limit, fault.fallback_polls,
                                              SegRescue{in, off, nseg, n, uint32_t(TILE)},
                                              hdr, fault.lookback_window, *sm.agg(i),
-                                             !ah && t != fault.never_publish_tile, sm.lb_scratch(i),
-                                             &carry);
+                                             !ah && t != fault.never_publish_tile, &carry);
             if (PERTURB && rc == 0) perturb(fault, t, kSitePrefix);
             if (lane == 0) {
                 if (rc == 0) {
