@@ -396,12 +396,23 @@ __device__ __forceinline__ uint32_t warp_lower_bound(const uint32_t *off, uint32
 // Returns 0 and the exclusive prefix of tile t in *carry_out; 1 if the
 // nearest terminal descriptor is poison; 2 if the poll limit ran out.
 
+// Back-off between a look-back's polls of a window: after the first
+// `after` polls, sleep `ns` before each further one (256 ns from the 256th
+// on).  Fewer polls leave L2 and the load/store path to the data streams;
+// more polls notice a publication sooner.
+struct Backoff {
+    uint32_t after;
+    uint32_t ns;
+};
+constexpr Backoff kBackoffDefault{8u, 64u};
+
 template <class Op, int K, class Rescue>
 __device__ __forceinline__ int lookback(uint64_t *desc, uint32_t t, uint32_t lane,
                                         uint32_t spin_limit, uint32_t fallback_polls,
                                         const Rescue &rescue, ScratchHeader *hdr,
                                         uint32_t window, uint32_t own, bool publish,
-                                        typename Op::T *carry_out) {
+                                        typename Op::T *carry_out,
+                                        const Backoff backoff = kBackoffDefault) {
     using T = typename Op::T;
     static_assert(Op::kCommutative, "the look-back combines per lane first");
     static_assert(K * 32 < (1 << 29), "window positions must fit the key");
@@ -462,7 +473,7 @@ __device__ __forceinline__ int lookback(uint64_t *desc, uint32_t t, uint32_t lan
                 }
                 continue;
             }
-            if (polls > 8) __nanosleep(polls > 256 ? 256 : 64);
+            if (polls > backoff.after) __nanosleep(polls > 256u ? 256u : backoff.ns);
 #pragma unroll
             for (int i = 0; i < K; ++i) {
                 const int64_t idx = base - 32 * i - static_cast<int64_t>(lane);

@@ -115,6 +115,16 @@ struct ScanConfig {
 #ifndef DWP_SCAN_AHEAD
 #define DWP_SCAN_AHEAD 2
 #endif
+// look-back back-off: sleep DWP_SCAN_LB_NS before every poll after the
+// first DWP_SCAN_LB_AFTER.  A look-back here starts when its tile is drawn
+// and polls while the tile loads; polling less often measured 7% faster at
+// 2^24 and 3.5% at 2^26 than the default (8 polls, then 64 ns)
+#ifndef DWP_SCAN_LB_AFTER
+#define DWP_SCAN_LB_AFTER 0
+#endif
+#ifndef DWP_SCAN_LB_NS
+#define DWP_SCAN_LB_NS 128
+#endif
 using ScanCfg = ScanConfig<DWP_SCAN_WARPS, DWP_SCAN_ITEMS, DWP_SCAN_IN, DWP_SCAN_OUT,
                            DWP_SCAN_RING, DWP_SCAN_LOOKERS, DWP_SCAN_LOOKK, DWP_SCAN_AHEAD>;
 
@@ -440,7 +450,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             if (early && rc == 0 && t != 0) {
                 perturb(fault, t, kSiteLookback);
                 rc = lookback<Op, C::kLookK>(desc, t, lane, fault.spin_limit, fault.fallback_polls,
-                                             ScanRescue<Op, TILE>{in, n}, hdr, 0u, 0u, false, &carry);
+                                             ScanRescue<Op, TILE>{in, n}, hdr, 0u, 0u, false, &carry,
+                                             Backoff{DWP_SCAN_LB_AFTER, DWP_SCAN_LB_NS});
             }
             // the tile's aggregate (or the reducer's verdict on it)
             w = warp_wait_or_end(sm.info_ready(i), (k / RING) & 1u, k, sm.end_iter());
@@ -454,7 +465,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 rc = lookback<Op, C::kLookK>(desc, t, lane, fault.spin_limit, fault.fallback_polls,
                                              ScanRescue<Op, TILE>{in, n}, hdr,
                                              fault.lookback_window, *sm.agg(i),
-                                             t != fault.never_publish_tile, &carry);
+                                             t != fault.never_publish_tile, &carry,
+                                             Backoff{DWP_SCAN_LB_AFTER, DWP_SCAN_LB_NS});
             }
             if (rc == 0) perturb(fault, t, kSitePrefix);
             if (lane == 0) {
