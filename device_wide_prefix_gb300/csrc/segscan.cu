@@ -65,7 +65,7 @@ struct SegConfig {
     static constexpr int kPrefixWords = kConsumers + kConsumers / 8;
     static constexpr int kPHeadWords = kConsumers / 4;  // one head byte per consumer thread
     static constexpr int kHeadWords = kTile / 32 + 1;   // tile head bitmap (+1 spill word)
-    // info slot: 3 mbarriers + pad (32 B); tile id, aggregate, carry,
+    // info slot: 4 mbarriers (32 B); tile id, aggregate, carry,
     // look-back result, aggregate head, first-row head, pad x2 (32 B);
     // prefix values; prefix head bytes; head bitmap; lane totals 33; lane
     // heads 33 (+ pad to 16 B)
@@ -104,6 +104,15 @@ struct SegConfig {
 #ifndef DWP_SEG_AHEAD
 #define DWP_SEG_AHEAD 1
 #endif
+#ifndef DWP_SEG_EARLY
+#define DWP_SEG_EARLY 1
+#endif
+#ifndef DWP_SEG_LB_AFTER
+#define DWP_SEG_LB_AFTER 0
+#endif
+#ifndef DWP_SEG_LB_NS
+#define DWP_SEG_LB_NS 128
+#endif
 using SegCfg = SegConfig<DWP_SEG_WARPS, DWP_SEG_ITEMS, DWP_SEG_IN, DWP_SEG_OUT, DWP_SEG_RING,
                          DWP_SEG_LOOKERS, DWP_SEG_LOOKK, DWP_SEG_AHEAD>;
 
@@ -123,6 +132,8 @@ struct SegSmem {
     __device__ uint64_t *info_ready(int i) const { return reinterpret_cast<uint64_t *>(info(i)); }
     __device__ uint64_t *carry_ready(int i) const { return info_ready(i) + 1; }
     __device__ uint64_t *info_free(int i) const { return info_ready(i) + 2; }
+    // the producer has written tile_id(i) (the tile is drawn)
+    __device__ uint64_t *drawn(int i) const { return info_ready(i) + 3; }
     __device__ uint32_t *tile_id(int i) const { return reinterpret_cast<uint32_t *>(info(i) + 32); }
     __device__ uint32_t *agg(int i) const { return tile_id(i) + 1; }
     __device__ uint32_t *carry(int i) const { return tile_id(i) + 2; }
@@ -221,6 +232,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     constexpr int SIN = C::kIn, SOUT = C::kOut, RING = C::kRing, LW = C::kLookers;
     constexpr int WE = C::kWarpElems;
     constexpr int AHEAD = C::kAhead;
+    constexpr bool EARLY = DWP_SEG_EARLY != 0;
     constexpr uint32_t NCONS = C::kConsumers;
     constexpr uint32_t kReducer0 = 1, kLooker0 = 1 + SIN, kReloader = 1 + SIN + LW,
                        kConsumer0 = 2 + SIN + LW;
@@ -253,6 +265,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             mbar_init(sm.info_ready(i), 1);
             mbar_init(sm.carry_ready(i), 1);
             mbar_init(sm.info_free(i), NW);
+            mbar_init(sm.drawn(i), 1);
             *sm.heads_dirty(i) = 1u;  // bitmaps start uninitialised
         }
         *sm.abort_flag() = 0;
@@ -297,6 +310,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                     else if (PERTURB) perturb(fault, t, kSiteDraw);
                 }
                 *reinterpret_cast<volatile uint32_t *>(sm.tile_id(gi)) = t;
+                mbar_arrive(sm.drawn(gi));  // the look-back may start now
                 ++taken;
                 if (t == kNoTile) {
                     drawn_all = true;
@@ -535,7 +549,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         bool draining = false;
         for (uint32_t k = j;; k += LW) {
             const int i = int(k % RING);
-            const int w = warp_wait_or_end(sm.info_ready(i), (k / RING) & 1u, k, sm.end_iter());
+            int w = EARLY ? warp_wait_or_end(sm.drawn(i), (k / RING) & 1u, k, sm.end_iter())
+                          : warp_wait_or_end(sm.info_ready(i), (k / RING) & 1u, k, sm.end_iter());
             if (w != 2) {
                 if (w == 0 && lane == 0) record_error(hdr, DWP_ERR_PIPELINE_TIMEOUT);
                 return;
@@ -546,15 +561,40 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 return;
             }
             if (!draining && ld_volatile_smem(sm.abort_flag()) != 0) draining = true;
+            // early: the look-back runs while the tile loads, before its heads
+            // are known, and its carry is dropped if the tile's first row is a
+            // head.  Only with the unbounded window: an intermediate carries
+            // the tile's own aggregate, which needs the reduce first.
+            const bool early = EARLY && fault.lookback_window == 0u;
             uint32_t carry = 0;
-            int rc = (draining || ld_volatile_smem(sm.lbres(i)) != 0u) ? 1 : 0;
+            int rc = draining ? 1 : 0, early_rc = 0;
+            if (early && rc == 0 && t != 0) {
+                if (PERTURB) perturb(fault, t, kSiteLookback);
+                early_rc = lookback<Op, C::kLookK>(desc, t, lane, fault.spin_limit, fault.fallback_polls,
+                                             SegRescue{in, off, nseg, n, uint32_t(TILE)}, hdr, 0u, 0u,
+                                             false, &carry, Backoff{DWP_SEG_LB_AFTER, DWP_SEG_LB_NS});
+            }
+            if (EARLY) {
+                w = warp_wait_or_end(sm.info_ready(i), (k / RING) & 1u, k, sm.end_iter());
+                if (w != 2) {
+                    if (w == 0 && lane == 0) record_error(hdr, DWP_ERR_PIPELINE_TIMEOUT);
+                    return;
+                }
+            }
+            if (ld_volatile_smem(sm.lbres(i)) != 0u) rc = 1;  // the reducer gave the tile up
             const bool ah = ld_volatile_smem(sm.agg_head(i)) != 0u;
-            if (PERTURB && rc == 0) perturb(fault, t, kSiteLookback);
-            if (rc == 0 && t != 0 && ld_volatile_smem(sm.first_head(i)) == 0u)
+            const bool fh = ld_volatile_smem(sm.first_head(i)) != 0u;
+            if (early) {
+                if (fh) carry = 0;  // the tile restarts at its first row: no carry
+                else if (rc == 0) rc = early_rc;
+            }
+            if (!early && rc == 0 && t != 0 && !fh) {
+                if (PERTURB) perturb(fault, t, kSiteLookback);
                 rc = lookback<Op, C::kLookK>(desc, t, lane, fault.spin_limit, fault.fallback_polls,
                                              SegRescue{in, off, nseg, n, uint32_t(TILE)},
                                              hdr, fault.lookback_window, *sm.agg(i),
                                              !ah && t != fault.never_publish_tile, &carry);
+            }
             if (PERTURB && rc == 0) perturb(fault, t, kSitePrefix);
             if (lane == 0) {
                 if (rc == 0) {
