@@ -162,6 +162,78 @@ class ClockSampler:
                 "window": "timed region" if inside else "last samples (timed region shorter than the sampling period)"}
 
 
+class NvmlClockSampler:
+    """SM clock, clock-event reasons and power read through NVML (ctypes) on a
+    thread every `period` seconds: a timed region of a few milliseconds gets
+    several samples, where nvidia-smi's 100 ms period gives one.  Reads only;
+    nothing is set.  `ok` is False when NVML cannot be loaded."""
+
+    # nvmlClocksEventReasons bits (nvml.h)
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, index: int, period: float = 0.0005):
+        import ctypes
+        import threading
+        self.ok = False
+        self.period = period
+        self.samples = []
+        self._stop = threading.Event()
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(h)) != 0:
+                return
+            reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            mx = ctypes.c_uint(0)
+            nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))  # NVML_CLOCK_SM
+        except (OSError, AttributeError):
+            return
+        self.max_mhz = float(mx.value)
+        self.ok = True
+
+        def run():
+            clk, rs, mw = ctypes.c_uint(0), ctypes.c_ulonglong(0), ctypes.c_uint(0)
+            while not self._stop.is_set():
+                if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and \
+                        reasons(h, ctypes.byref(rs)) == 0:
+                    nv.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw))
+                    self.samples.append((time.time(), float(clk.value), int(rs.value), mw.value / 1e3))
+                time.sleep(period)
+
+        self._thread = threading.Thread(target=run, daemon=True)
+        self._thread.start()
+
+    def stop(self):
+        if self.ok:
+            self._stop.set()
+            self._thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float) -> dict | None:
+        used = [s for s in self.samples if t0 <= s[0] <= t1]
+        if not used:
+            return None
+        reasons = sorted({name for s in used for bit, name in self.REASONS.items() if s[2] & bit})
+        return {"sm_mhz": float(np.median([s[1] for s in used])), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(used), "power_w_max": max(s[3] for s in used),
+                "window": "timed region", "source": "NVML, %.1f ms period" % (self.period * 1e3)}
+
+
+def clock_record(nvml, smi, t0: float, t1: float) -> dict | None:
+    """The NVML samples of the timed region when there are any, else the
+    nvidia-smi ones; the other source's summary rides along."""
+    a = nvml.summary(t0, t1) if nvml is not None and nvml.ok else None
+    b = smi.summary(t0, t1) if smi is not None else None
+    if a is None:
+        return b
+    if b is not None:
+        a["nvidia_smi"] = {k: b.get(k) for k in ("sm_mhz", "reasons", "samples")}
+    return a
+
+
 def max_over_ranks(dist, v: float, device) -> float:
     """The largest of every rank's v (a time), through one all-reduce on
     `device` (the GPU under NCCL; the CPU under gloo).  With dist None (one
@@ -299,6 +371,7 @@ def main() -> None:
             raise RuntimeError(dwp.status_string(st))
 
     clocks = ClockSampler(local_rank) if rank == 0 else None
+    nvml_clocks = NvmlClockSampler(local_rank) if rank == 0 else None
     for _ in range(args.warmup):
         step()
     barrier()
@@ -399,6 +472,8 @@ def main() -> None:
     del xs, ys, scr2
     if clocks is not None:
         clocks.stop()
+    if nvml_clocks is not None:
+        nvml_clocks.stop()
 
     peaks = measured_peaks()
     alg_bytes = 8 * n
@@ -446,7 +521,7 @@ def main() -> None:
                 "how": "pinned host in and out, two steps in flight on two streams",
                 "serial_one_stream_ms_per_step": e2e_serial_ms},
         "gpu_launches": 2 * args.steps,
-        "clocks": clocks.summary(wall0, wall1) if clocks is not None else None,
+        "clocks": clock_record(nvml_clocks, clocks, wall0, wall1),
         "secondary": secondary,
     }
     print(json.dumps(line), flush=True)
