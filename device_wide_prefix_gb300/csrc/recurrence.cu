@@ -104,9 +104,6 @@ struct RecConfig {
 #ifndef DWP_REC_AHEAD
 #define DWP_REC_AHEAD 2
 #endif
-#ifndef DWP_REC_EARLY
-#define DWP_REC_EARLY 1
-#endif
 #ifndef DWP_REC_LB_AFTER
 #define DWP_REC_LB_AFTER 0
 #endif
@@ -347,7 +344,6 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     constexpr int NW = C::kWarps, ITEMS = C::kItems, TILE = C::kTile;
     constexpr int SIN = C::kIn, SOUT = C::kOut, RING = C::kRing, LW = C::kLookers;
     constexpr int WE = C::kWarpElems, AHEAD = C::kAhead;
-    constexpr bool EARLY = DWP_REC_EARLY != 0;
     constexpr uint32_t NCONS = C::kConsumers;
     constexpr uint32_t kReducer0 = 1, kLooker0 = 1 + SIN, kReloader = 1 + SIN + LW,
                        kConsumer0 = 2 + SIN + LW;
@@ -589,10 +585,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         bool draining = false;
         for (uint32_t k = j;; k += LW) {
             const int i = int(k % RING);
-            // EARLY: the look-back reads only predecessors' descriptors, so it
+            // the look-back reads only predecessors' descriptors, so it
             // starts when the tile is drawn and runs while the tile loads
-            int w = EARLY ? warp_wait_or_end(sm.drawn(i), (k / RING) & 1u, k, sm.end_iter())
-                          : warp_wait_or_end(sm.info_ready(i), (k / RING) & 1u, k, sm.end_iter());
+            int w = warp_wait_or_end(sm.drawn(i), (k / RING) & 1u, k, sm.end_iter());
             if (w != 2) {
                 if (w == 0 && lane == 0) record_error(hdr, DWP_ERR_PIPELINE_TIMEOUT);
                 return;
@@ -605,25 +600,17 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             if (!draining && ld_volatile_smem(sm.abort_flag()) != 0) draining = true;
             float carry = 0.0f;
             int rc = draining ? 1 : 0;
-            if (EARLY) {
-                if (PERTURB && rc == 0) perturb(fault, t, kSiteLookback);
-                if (rc == 0 && t != 0)
-                    rc = lookback_affine(desc, t, lane, fault.spin_limit, fault.fallback_polls, rescue,
-                                         &hdr->fallbacks, &carry, backoff);
-                // the tile's own map (or the reducer's verdict on it)
-                w = warp_wait_or_end(sm.info_ready(i), (k / RING) & 1u, k, sm.end_iter());
-                if (w != 2) {
-                    if (w == 0 && lane == 0) record_error(hdr, DWP_ERR_PIPELINE_TIMEOUT);
-                    return;
-                }
-                if (ld_volatile_smem(sm.lbres(i)) != 0u) rc = 1;
-            } else {
-                if (ld_volatile_smem(sm.lbres(i)) != 0u) rc = 1;
-                if (PERTURB && rc == 0) perturb(fault, t, kSiteLookback);
-                if (rc == 0 && t != 0)
-                    rc = lookback_affine(desc, t, lane, fault.spin_limit, fault.fallback_polls, rescue,
-                                         &hdr->fallbacks, &carry, backoff);
+            if (PERTURB && rc == 0) perturb(fault, t, kSiteLookback);
+            if (rc == 0 && t != 0)
+                rc = lookback_affine(desc, t, lane, fault.spin_limit, fault.fallback_polls, rescue,
+                                     &hdr->fallbacks, &carry, backoff);
+            // the tile's own map (or the reducer's verdict on it)
+            w = warp_wait_or_end(sm.info_ready(i), (k / RING) & 1u, k, sm.end_iter());
+            if (w != 2) {
+                if (w == 0 && lane == 0) record_error(hdr, DWP_ERR_PIPELINE_TIMEOUT);
+                return;
             }
+            if (ld_volatile_smem(sm.lbres(i)) != 0u) rc = 1;
             if (PERTURB && rc == 0) perturb(fault, t, kSitePrefix);
             if (lane == 0) {
                 if (rc == 0) {

@@ -25,8 +25,10 @@
 //   * per-thread totals and their exclusive prefix are (head, value) pairs;
 //   * a tile holding a head publishes its inclusive prefix at once (its value
 //     after its last head is final); the look-back is a plain u32-add
-//     look-back that stops at the nearest prefix, and runs only if the
-//     tile's first row is not itself a head;
+//     look-back that stops at the nearest prefix.  It starts when the tile
+//     is drawn, before its heads are known, and its carry is dropped if the
+//     tile's first row is a head (with a bounded window it waits for the
+//     reduce and runs only when the first row is not a head);
 //   * rows outside [offsets[0], min(offsets[N], n)) are not written.
 // Offsets are trusted (no readback, "Limitations"): unordered offsets give
 // unspecified values but every access stays inside offsets[0..N].
@@ -104,9 +106,9 @@ struct SegConfig {
 #ifndef DWP_SEG_AHEAD
 #define DWP_SEG_AHEAD 1
 #endif
-#ifndef DWP_SEG_EARLY
-#define DWP_SEG_EARLY 1
-#endif
+// look-back back-off: sleep DWP_SEG_LB_NS before every poll after the first
+// DWP_SEG_LB_AFTER (as in the plain scan: the look-back starts at the draw
+// and polls while the tile loads)
 #ifndef DWP_SEG_LB_AFTER
 #define DWP_SEG_LB_AFTER 0
 #endif
@@ -232,7 +234,6 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     constexpr int SIN = C::kIn, SOUT = C::kOut, RING = C::kRing, LW = C::kLookers;
     constexpr int WE = C::kWarpElems;
     constexpr int AHEAD = C::kAhead;
-    constexpr bool EARLY = DWP_SEG_EARLY != 0;
     constexpr uint32_t NCONS = C::kConsumers;
     constexpr uint32_t kReducer0 = 1, kLooker0 = 1 + SIN, kReloader = 1 + SIN + LW,
                        kConsumer0 = 2 + SIN + LW;
@@ -549,8 +550,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         bool draining = false;
         for (uint32_t k = j;; k += LW) {
             const int i = int(k % RING);
-            int w = EARLY ? warp_wait_or_end(sm.drawn(i), (k / RING) & 1u, k, sm.end_iter())
-                          : warp_wait_or_end(sm.info_ready(i), (k / RING) & 1u, k, sm.end_iter());
+            int w = warp_wait_or_end(sm.drawn(i), (k / RING) & 1u, k, sm.end_iter());
             if (w != 2) {
                 if (w == 0 && lane == 0) record_error(hdr, DWP_ERR_PIPELINE_TIMEOUT);
                 return;
@@ -565,21 +565,21 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             // are known, and its carry is dropped if the tile's first row is a
             // head.  Only with the unbounded window: an intermediate carries
             // the tile's own aggregate, which needs the reduce first.
-            const bool early = EARLY && fault.lookback_window == 0u;
+            const bool early = fault.lookback_window == 0u;
             uint32_t carry = 0;
             int rc = draining ? 1 : 0, early_rc = 0;
             if (early && rc == 0 && t != 0) {
                 if (PERTURB) perturb(fault, t, kSiteLookback);
                 early_rc = lookback<Op, C::kLookK>(desc, t, lane, fault.spin_limit, fault.fallback_polls,
-                                             SegRescue{in, off, nseg, n, uint32_t(TILE)}, hdr, 0u, 0u,
-                                             false, &carry, Backoff{DWP_SEG_LB_AFTER, DWP_SEG_LB_NS});
+                                                   SegRescue{in, off, nseg, n, uint32_t(TILE)}, hdr, 0u,
+                                                   0u, false, &carry,
+                                                   Backoff{DWP_SEG_LB_AFTER, DWP_SEG_LB_NS});
             }
-            if (EARLY) {
-                w = warp_wait_or_end(sm.info_ready(i), (k / RING) & 1u, k, sm.end_iter());
-                if (w != 2) {
-                    if (w == 0 && lane == 0) record_error(hdr, DWP_ERR_PIPELINE_TIMEOUT);
-                    return;
-                }
+            // the tile's heads and aggregate (or the reducer's verdict on it)
+            w = warp_wait_or_end(sm.info_ready(i), (k / RING) & 1u, k, sm.end_iter());
+            if (w != 2) {
+                if (w == 0 && lane == 0) record_error(hdr, DWP_ERR_PIPELINE_TIMEOUT);
+                return;
             }
             if (ld_volatile_smem(sm.lbres(i)) != 0u) rc = 1;  // the reducer gave the tile up
             const bool ah = ld_volatile_smem(sm.agg_head(i)) != 0u;
