@@ -29,6 +29,7 @@ DWP_ERR_CUDA = 5
 DWP_ERR_LOOKBACK_TIMEOUT = 6
 DWP_ERR_PIPELINE_TIMEOUT = 7
 DWP_ERR_NO_DEVICE = 8
+DWP_ERR_BOUNDS = 9
 
 DWP_U32_ADD = 0
 DWP_F32_ADD = 1

@@ -317,6 +317,7 @@ const char *dwp_status_string(dwp_status status) {
         case DWP_ERR_LOOKBACK_TIMEOUT: return "DWP_ERR_LOOKBACK_TIMEOUT";
         case DWP_ERR_PIPELINE_TIMEOUT: return "DWP_ERR_PIPELINE_TIMEOUT";
         case DWP_ERR_NO_DEVICE: return "DWP_ERR_NO_DEVICE";
+        case DWP_ERR_BOUNDS: return "DWP_ERR_BOUNDS";
     }
     return "DWP_UNKNOWN_STATUS";
 }

@@ -228,6 +228,23 @@ __device__ __forceinline__ void record_error(ScratchHeader *hdr, uint32_t code) 
     atomicCAS(&hdr->status, 0u, code);
 }
 
+// Debug bounds build (compile with -DDWP_DEBUG_BOUNDS=1).  Before each
+// global access, the plain-scan kernels ask whether elements [first,
+// first + count) lie inside a buffer of `extent` elements.  An access that
+// would leave its buffer is skipped and DWP_ERR_BOUNDS is recorded in the
+// status word: a checked run reports a bad index instead of faulting.  The
+// default build compiles every check to `true`.
+#ifndef DWP_DEBUG_BOUNDS
+#define DWP_DEBUG_BOUNDS 0
+#endif
+__device__ __forceinline__ bool in_bounds(ScratchHeader *hdr, uint64_t first, uint64_t count,
+                                          uint64_t extent) {
+    if (!DWP_DEBUG_BOUNDS) return true;
+    if (first <= extent && count <= extent - first) return true;
+    record_error(hdr, DWP_ERR_BOUNDS);
+    return false;
+}
+
 // ---------------------------------------------------------------------------
 // Schedule perturbation, a test hook (dwp_debug_set_delay).  A missing
 // ordering or synchronisation in a chained scan shows up only under rare

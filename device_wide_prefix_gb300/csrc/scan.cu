@@ -176,11 +176,12 @@ struct ScanSmem {
 // a ragged tile's bulk part come this way.
 template <class Op>
 __device__ __forceinline__ uint4 tail_vec(const typename Op::T *in, uint64_t base, uint32_t pos,
-                                          uint32_t valid) {
+                                          uint32_t valid, ScratchHeader *hdr, uint64_t n) {
     uint32_t w[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e)
-        w[e] = pos + e < valid ? Op::to_bits(in[base + pos + e]) : Op::to_bits(Op::identity());
+        w[e] = pos + e < valid && in_bounds(hdr, base + pos + e, 1, n) ? Op::to_bits(in[base + pos + e])
+                                                                      : Op::to_bits(Op::identity());
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
@@ -274,7 +275,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 } else if (AHEAD > 0) {
                     uint32_t valid, bulk;
                     tile_extent(t, valid, bulk);
-                    if (bulk) bulk_prefetch_l2(in + uint64_t(t) * TILE, bulk * 4u, keep);
+                    if (bulk && in_bounds(hdr, uint64_t(t) * TILE, bulk, n))
+                        bulk_prefetch_l2(in + uint64_t(t) * TILE, bulk * 4u, keep);
                 }
             }
             if (ok && k >= uint32_t(SIN))
@@ -284,7 +286,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 // tiles drawn but never loaded: poison them so no successor waits
                 for (uint32_t g = k; g < taken; ++g) {
                     const uint32_t t = ld_volatile_smem(sm.tile_id(int(g % RING)));
-                    if (t != kNoTile) st_relaxed_gpu(desc + t, make_desc(kPoison, 0u));
+                    if (t != kNoTile && in_bounds(hdr, t, 1, num_tiles))
+                        st_relaxed_gpu(desc + t, make_desc(kPoison, 0u));
                 }
                 stop_at(k - 1);  // buffers still in use: leave them alone
                 return;
@@ -296,7 +299,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             }
             uint32_t valid, bulk;
             tile_extent(t, valid, bulk);
-            if (bulk) {
+            if (bulk && in_bounds(hdr, uint64_t(t) * TILE, bulk, n) && in_bounds(hdr, 0, bulk, TILE)) {
                 mbar_arrive_expect_tx(sm.in_full(s), bulk * 4u);
                 bulk_load_hint(sm.in_data(s), in + uint64_t(t) * TILE, bulk * 4u, sm.in_full(s), keep);
             } else {
@@ -324,7 +327,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             if (ld_volatile_smem(sm.abort_flag()) != 0) {
                 // an earlier tile of this block gave up: poison this one
                 if (lane == 0) {
-                    st_relaxed_gpu(desc + t, make_desc(kPoison, 0u));
+                    if (in_bounds(hdr, t, 1, num_tiles)) st_relaxed_gpu(desc + t, make_desc(kPoison, 0u));
                     *sm.lbres(i) = 1u;
                     mbar_arrive(sm.in_empty(s));
                     mbar_arrive(sm.info_ready(i));
@@ -369,7 +372,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 #pragma unroll
                     for (int v = 0; v < ITEMS / 4; ++v) {
                         const uint32_t pos = p0 + 4u * v;
-                        const uint4 q = pos < bulk ? v4[c * (ITEMS / 4) + v] : tail_vec<Op>(in, base, pos, valid);
+                        const uint4 q = pos < bulk ? v4[c * (ITEMS / 4) + v] : tail_vec<Op>(in, base, pos, valid, hdr, n);
                         acc = Op::combine(acc, Op::combine(Op::combine(Op::from_bits(q.x), Op::from_bits(q.y)),
                                                            Op::combine(Op::from_bits(q.z), Op::from_bits(q.w))));
                     }
@@ -410,7 +413,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             // publish the aggregate at once (tile 0: its inclusive prefix)
             perturb(fault, t, kSiteAggregate);
             if (lane == 0) {
-                if (t != fault.never_publish_tile)
+                if (t != fault.never_publish_tile && in_bounds(hdr, t, 1, num_tiles))
                     st_relaxed_gpu(desc + t, make_desc(t == 0 ? kPrefix : kAggregate, Op::to_bits(agg)));
                 *sm.agg(i) = Op::to_bits(agg);
                 *sm.lbres(i) = 0u;
@@ -470,7 +473,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             }
             if (rc == 0) perturb(fault, t, kSitePrefix);
             if (lane == 0) {
-                if (rc == 0) {
+                if (!in_bounds(hdr, t, 1, num_tiles)) {
+                    // debug bounds build only: no descriptor to publish
+                } else if (rc == 0) {
                     if (t != 0 && t != fault.never_publish_tile)
                         st_relaxed_gpu(desc + t, make_desc(kPrefix, Op::to_bits(Op::combine(carry, Op::from_bits(*sm.agg(i))))));
                 } else {
@@ -515,7 +520,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             }
             uint32_t valid, bulk;
             tile_extent(t, valid, bulk);
-            if (bulk) {
+            if (bulk && in_bounds(hdr, uint64_t(t) * TILE, bulk, n) && in_bounds(hdr, 0, bulk, TILE)) {
                 mbar_arrive_expect_tx(sm.out_full(o), bulk * 4u);
                 bulk_load_hint(sm.out_data(o), in + uint64_t(t) * TILE, bulk * 4u, sm.out_full(o),
                                l2_policy_evict_first());
@@ -591,7 +596,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             for (int v = 0; v < ITEMS / 4; ++v) {
                 const uint32_t pos = p0 + 4u * v;
                 const bool staged = pos < bulk;
-                const uint4 q = staged ? v4[v] : tail_vec<Op>(in, base, pos, valid);
+                const uint4 q = staged ? v4[v] : tail_vec<Op>(in, base, pos, valid, hdr, n);
                 const uint32_t qq[4] = {q.x, q.y, q.z, q.w};
                 uint32_t r[4];
 #pragma unroll
@@ -610,7 +615,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 } else {
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        if (pos + e < valid) out[base + pos + e] = Op::from_bits(r[e]);
+                        if (pos + e < valid && in_bounds(hdr, base + pos + e, 1, n))
+                            out[base + pos + e] = Op::from_bits(r[e]);
                 }
             }
         }
@@ -619,7 +625,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         if (lane == 0) {
             const uint32_t w0 = cw * WE;
             const uint32_t w1 = min(w0 + uint32_t(WE), bulk);
-            if (w1 > w0) {
+            if (w1 > w0 && in_bounds(hdr, base + w0, w1 - w0, n)) {
                 bulk_store_hint(out + base + w0, buf + w0, (w1 - w0) * 4u, l2_policy_evict_first());
                 bulk_commit();
                 bulk_wait_read<1>();

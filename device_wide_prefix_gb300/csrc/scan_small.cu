@@ -85,7 +85,7 @@ __global__ void __launch_bounds__(kSmallThreads, 2)
             const uint64_t rem = n - uint64_t(t) * TILE;
             valid = rem < uint64_t(TILE) ? uint32_t(rem) : TILE;
             bulk = valid & ~3u;  // the bulk copy moves whole 16-byte vectors
-            if (bulk) {
+            if (bulk && in_bounds(hdr, uint64_t(t) * TILE, bulk, n) && in_bounds(hdr, 0, bulk, TILE)) {
                 mbar_arrive_expect_tx(full, bulk * 4u);
                 bulk_load(stage, in + uint64_t(t) * TILE, bulk * 4u, full);
             } else {
@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(kSmallThreads, 2)
             bool ok = mbar_wait(full, 0, kPipeWaitLimit);
             if (!ok) {
                 mbar_wait(full, 0, kPipeWaitLimit);
-                st_relaxed_gpu(desc + t, make_desc(kPoison, 0u));
+                if (in_bounds(hdr, t, 1, num_tiles)) st_relaxed_gpu(desc + t, make_desc(kPoison, 0u));
                 record_error(hdr, DWP_ERR_PIPELINE_TIMEOUT);
             }
             s_ok = ok ? 1u : 0u;
@@ -126,7 +126,8 @@ __global__ void __launch_bounds__(kSmallThreads, 2)
             uint32_t e[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-                e[j] = pos + j < valid ? Op::to_bits(in[base + pos + j]) : Op::to_bits(Op::identity());
+                e[j] = pos + j < valid && in_bounds(hdr, base + pos + j, 1, n) ? Op::to_bits(in[base + pos + j])
+                                                                                 : Op::to_bits(Op::identity());
             w = make_uint4(e[0], e[1], e[2], e[3]);
         }
         v[4 * q + 0] = Op::from_bits(w.x);
@@ -162,7 +163,7 @@ __global__ void __launch_bounds__(kSmallThreads, 2)
     // -- publish the aggregate, look back, publish the prefix -------------
     if (warp == 0) {
         perturb(fault, t, kSiteAggregate);
-        if (lane == 0 && t != fault.never_publish_tile)
+        if (lane == 0 && t != fault.never_publish_tile && in_bounds(hdr, t, 1, num_tiles))
             st_relaxed_gpu(desc + t, make_desc(t == 0 ? kPrefix : kAggregate, Op::to_bits(agg)));
         perturb(fault, t, kSiteLookback);
         T carry = Op::identity();
@@ -175,7 +176,9 @@ __global__ void __launch_bounds__(kSmallThreads, 2)
                                                    t != fault.never_publish_tile, &carry);
         if (rc == 0) perturb(fault, t, kSitePrefix);
         if (lane == 0) {
-            if (rc == 0) {
+            if (!in_bounds(hdr, t, 1, num_tiles)) {
+                // debug bounds build only: no descriptor to publish
+            } else if (rc == 0) {
                 if (t != 0 && t != fault.never_publish_tile)
                     st_relaxed_gpu(desc + t, make_desc(kPrefix, Op::to_bits(Op::combine(carry, agg))));
             } else {
@@ -213,12 +216,13 @@ __global__ void __launch_bounds__(kSmallThreads, 2)
         } else {
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-                if (pos + j < valid) out[base + pos + j] = Op::from_bits(y[j]);
+                if (pos + j < valid && in_bounds(hdr, base + pos + j, 1, n))
+                    out[base + pos + j] = Op::from_bits(y[j]);
         }
     }
     fence_proxy_async_smem();  // the bulk store reads the stage through the async proxy
     __syncthreads();
-    if (threadIdx.x == 0 && bulk) {
+    if (threadIdx.x == 0 && bulk && in_bounds(hdr, base, bulk, n)) {
         bulk_store(out + base, stage, bulk * 4u);
         bulk_commit();
         bulk_wait_all<0>();

@@ -63,7 +63,9 @@ typedef enum dwp_status {
     DWP_ERR_CUDA = 5,              /* a CUDA runtime call or launch failed */
     DWP_ERR_LOOKBACK_TIMEOUT = 6,  /* device: a look-back spin ran past its limit */
     DWP_ERR_PIPELINE_TIMEOUT = 7,  /* device: a shared-memory pipeline wait ran past its limit */
-    DWP_ERR_NO_DEVICE = 8          /* no usable CUDA device */
+    DWP_ERR_NO_DEVICE = 8,         /* no usable CUDA device */
+    DWP_ERR_BOUNDS = 9             /* device, debug bounds build only: an access would have
+                                      left its buffer and was skipped (never in the default build) */
 } dwp_status;
 
 /* Associative operators of the plain scans. */

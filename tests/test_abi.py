@@ -40,9 +40,10 @@ def test_exports_every_declared_symbol(lib):
 
 def test_version_and_status_strings(lib):
     assert dwp.dwp_version() >= 100
-    for code in range(9):
+    for code in range(10):
         s = dwp.dwp_status_string(code)
         assert s.startswith("DWP_") and "UNKNOWN" not in s
+    assert dwp.dwp_status_string(dwp.DWP_ERR_BOUNDS) == "DWP_ERR_BOUNDS"
     assert "UNKNOWN" in dwp.dwp_status_string(99)
 
 

@@ -1,0 +1,113 @@
+"""The plain scan in the debug bounds build (-DDWP_DEBUG_BOUNDS=1): every
+global access of both scan kernels is checked against its buffer first, and
+an access that would leave it is skipped and reported as DWP_ERR_BOUNDS
+instead of being made.  Run over the sizes where index arithmetic is most
+likely to slip (tile and tier edges, ragged tails, the switch between the
+two kernels, in place, a rescued tile, a bounded window), the checked build
+must report no bounds error and still match the oracle."""
+import ctypes
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import device_wide_prefix_gb300 as dwp  # noqa: E402
+from device_wide_prefix_gb300 import build as dwp_build  # noqa: E402
+
+BOUNDS_LIB = os.path.join(os.path.dirname(dwp.__file__), "libdwp_bounds.so")
+LARGE_TILE = 7168
+SMALL_MAX = 1 << 23
+OPS = {"u32_add": dwp.DWP_U32_ADD, "f32_add": dwp.DWP_F32_ADD, "u32_max": dwp.DWP_U32_MAX}
+
+
+@pytest.fixture(scope="module")
+def lib():
+    dwp_build.build(extra=["-DDWP_DEBUG_BOUNDS=1"], lib=BOUNDS_LIB)
+    return dwp.load(BOUNDS_LIB)
+
+
+@pytest.fixture(scope="module")
+def ref():
+    return oracle.Oracle()
+
+
+def run(lib, x, op, inclusive, inplace=False):
+    """One call of the checked library; returns (output, device status)."""
+    t = torch.from_numpy(x.view(np.float32 if op == "f32_add" else np.int32)).cuda()
+    y = t if inplace else torch.empty_like(t)
+    sb = ctypes.c_size_t(0)
+    entry = lib.dwp_scan_inclusive if inclusive else lib.dwp_scan_exclusive
+    assert entry(OPS[op], None, None, x.size, None, ctypes.byref(sb), None) == dwp.DWP_SUCCESS
+    scratch = torch.empty(max(sb.value, 16), dtype=torch.uint8, device="cuda")
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    st = entry(OPS[op], ctypes.c_void_p(t.data_ptr()), ctypes.c_void_p(y.data_ptr()), x.size,
+               ctypes.c_void_p(scratch.data_ptr()), ctypes.byref(sb), stream)
+    assert st == dwp.DWP_SUCCESS
+    status = lib.dwp_read_status(ctypes.c_void_p(scratch.data_ptr()), stream)
+    return y.cpu().numpy().view(x.dtype), status
+
+
+def check(ref, x, op, inclusive, y):
+    if op == "f32_add":
+        yr, ab = ref.scan_f32_add(x, inclusive)
+        assert (np.abs(y.astype(np.float64) - yr) <= 1e-4 * ab + 1e-6).all()
+    else:
+        assert np.array_equal(y, ref.scan(op, x, inclusive))
+
+
+def values(n, op, seed):
+    return synth.f32_values(n, seed) if op == "f32_add" else synth.u32_full_values(n, seed)
+
+
+SIZES = (1, 3, 4, 5, 3071, 3072, 3073, (1 << 18) + 1, 7167, 7168 * 50 + 3, (1 << 20) + 1,
+         15360 * 70 - 1, SMALL_MAX - 1, SMALL_MAX, SMALL_MAX + 1, LARGE_TILE * 1500 + 4097)
+
+
+@pytest.mark.parametrize("op", sorted(OPS))
+@pytest.mark.parametrize("inclusive", [False, True])
+def test_no_bounds_error_at_tile_and_tier_edges(lib, ref, op, inclusive):
+    for n in SIZES:
+        x = values(n, op, 900 + n % 89)
+        y, status = run(lib, x, op, inclusive)
+        assert status == dwp.DWP_SUCCESS, (n, dwp.status_string(status))
+        check(ref, x, op, inclusive, y)
+
+
+@pytest.mark.parametrize("n", [7168 * 50 + 9, LARGE_TILE * 1500 + 9])
+def test_no_bounds_error_in_place(lib, ref, n):
+    x = values(n, "u32_add", 7)
+    y, status = run(lib, x.copy(), "u32_add", False, inplace=True)
+    assert status == dwp.DWP_SUCCESS
+    check(ref, x, "u32_add", False, y)
+
+
+@pytest.mark.parametrize("n", [15360 * 100 + 77, LARGE_TILE * 1500 + 77])
+def test_no_bounds_error_with_a_rescued_tile_and_a_window(lib, ref, n):
+    """The Decoupled Fallback reads a tile from the input, and a bounded
+    window publishes intermediates: both paths under the checks."""
+    x = values(n, "u32_add", 8)
+    try:
+        lib.dwp_debug_set_fault(7, 0, 64)
+        y, status = run(lib, x, "u32_add", True)
+        assert status == dwp.DWP_SUCCESS
+        check(ref, x, "u32_add", True, y)
+        assert lib.dwp_set_lookback_window(32) == dwp.DWP_SUCCESS
+        y, status = run(lib, x, "u32_add", True)
+        assert status == dwp.DWP_SUCCESS
+        check(ref, x, "u32_add", True, y)
+    finally:
+        lib.dwp_set_lookback_window(0)
+        lib.dwp_debug_set_fault(0xFFFFFFFF, 0, 0)
+
+
+def test_the_default_library_is_not_the_checked_one(lib):
+    assert os.path.abspath(dwp.LIB_PATH) != os.path.abspath(BOUNDS_LIB)
