@@ -136,9 +136,10 @@ __device__ __forceinline__ uint32_t nonzero_bytes4(uint32_t x) {
 // Keep flag of record pos of a tile: from the slot below `fbulk`, from global
 // memory below `valid`, else 0.
 __device__ __forceinline__ bool keep_at(const unsigned char *sflags, const uint8_t *gflags,
-                                        uint64_t base, uint32_t pos, uint32_t fbulk, uint32_t valid) {
+                                        uint64_t base, uint32_t pos, uint32_t fbulk, uint32_t valid,
+                                        ScratchHeader *hdr, uint64_t n) {
     if (pos < fbulk) return sflags[pos] != 0;
-    if (pos < valid) return gflags[base + pos] != 0;
+    if (pos < valid && in_bounds(hdr, base + pos, 1, n)) return gflags[base + pos] != 0;
     return false;
 }
 
@@ -241,8 +242,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             uint32_t valid, fbulk;
             tile_extent(t, valid, fbulk);
             const uint64_t base = uint64_t(t) * TILE;
-            if (DWP_CMP_PREFETCH == 1) bulk_prefetch_l2(recs + base, valid * 16u, keep);
-            if (fbulk) {
+            if (DWP_CMP_PREFETCH == 1 && in_bounds(hdr, base, valid, n))
+                bulk_prefetch_l2(recs + base, valid * 16u, keep);
+            if (fbulk && in_bounds(hdr, base, fbulk, n) && in_bounds(hdr, 0, fbulk, C::kFlagBytes)) {
                 mbar_arrive_expect_tx(sm.flags_full(i), fbulk);
                 bulk_load(sm.flags(i), flags + base, fbulk, sm.flags_full(i));
             } else {
@@ -270,7 +272,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             if (!draining && ld_volatile_smem(sm.abort_flag()) != 0) draining = true;
             if (draining) {
                 if (lane == 0) {
-                    st_relaxed_gpu(desc + t, make_desc(kPoison, 0u));
+                    if (in_bounds(hdr, t, 1, num_tiles)) st_relaxed_gpu(desc + t, make_desc(kPoison, 0u));
                     *sm.lbres(i) = 1u;
                     mbar_arrive(sm.carry_ready(i));
                 }
@@ -319,7 +321,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                     const uint32_t p0 = (lane * PER + j) * IT;
                     uint32_t m = 0;
                     for (int q = 0; q < IT; ++q)
-                        if (keep_at(sf, flags, base, p0 + q, fbulk, valid)) m |= 1u << q;
+                        if (keep_at(sf, flags, base, p0 + q, fbulk, valid, hdr, n)) m |= 1u << q;
                     cntm[j] = uint32_t(__popc(m)) | (m << 24);
                 }
             }
@@ -344,9 +346,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             for (int q = 0; q < PER; ++q)
                 pre[prefix_slot(lane * PER + q)] = (lane_excl + mine[q]) | (cntm[q] & 0xff000000u);
             perturb(fault, t, kSiteAggregate);
-            if (lane == 0 && t != fault.never_publish_tile)
+            if (lane == 0 && t != fault.never_publish_tile && in_bounds(hdr, t, 1, num_tiles))
                 st_relaxed_gpu(desc + t, make_desc(t == 0 ? kPrefix : kAggregate, total));
-            if (DWP_CMP_PREFETCH == 2 && lane == 0 && total != 0u)
+            if (DWP_CMP_PREFETCH == 2 && lane == 0 && total != 0u && in_bounds(hdr, base, valid, n))
                 bulk_prefetch_l2(recs + base, valid * 16u, l2_policy_evict_last());
             uint32_t carry = 0;
             int rc = 0;
@@ -357,10 +359,12 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                                              fault.lookback_window, total,
                                              t != fault.never_publish_tile, &carry);
             if (rc == 0) perturb(fault, t, kSitePrefix);
-            if (DWP_CMP_PREFETCH == 3 && lane == 0 && rc == 0 && total != 0u)
+            if (DWP_CMP_PREFETCH == 3 && lane == 0 && rc == 0 && total != 0u && in_bounds(hdr, base, valid, n))
                 bulk_prefetch_l2(recs + base, valid * 16u, l2_policy_evict_last());
             if (lane == 0) {
-                if (rc == 0) {
+                if (!in_bounds(hdr, t, 1, num_tiles)) {
+                    // debug bounds build only: no descriptor to publish
+                } else if (rc == 0) {
                     if (t != 0 && t != fault.never_publish_tile)
                         st_relaxed_gpu(desc + t, make_desc(kPrefix, carry + total));
                     if (t == num_tiles - 1) *count = carry + total;  // K4: output length
@@ -408,8 +412,12 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             }
             uint32_t valid, fbulk;
             tile_extent(t, valid, fbulk);
-            mbar_arrive_expect_tx(sm.out_full(o), valid * 16u);
-            bulk_load_hint(sm.recs(o), recs + uint64_t(t) * TILE, valid * 16u, sm.out_full(o), drop);
+            if (in_bounds(hdr, uint64_t(t) * TILE, valid, n) && in_bounds(hdr, 0, valid, TILE)) {
+                mbar_arrive_expect_tx(sm.out_full(o), valid * 16u);
+                bulk_load_hint(sm.recs(o), recs + uint64_t(t) * TILE, valid * 16u, sm.out_full(o), drop);
+            } else {
+                mbar_arrive(sm.out_full(o));
+            }
         }
     }
 
@@ -456,7 +464,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         __syncwarp();
         if (lane == 0) {
             mbar_arrive(sm.info_free(i));  // flags and prefixes have been read
-            if (nkeep) {
+            if (nkeep && in_bounds(hdr, first, nkeep, n) && in_bounds(hdr, 0, nkeep, WR)) {
                 bulk_store_hint(out + first, sm.recs(o) + cw * WR, nkeep * 16u, drop);
                 bulk_commit();
                 bulk_wait_read<1>();

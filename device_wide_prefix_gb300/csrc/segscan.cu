@@ -173,9 +173,10 @@ struct SegSmem {
 };
 
 __device__ __forceinline__ uint32_t seg_elem(const uint32_t *buf, const uint32_t *in, uint64_t base,
-                                             uint32_t pos, uint32_t bulk, uint32_t valid) {
+                                             uint32_t pos, uint32_t bulk, uint32_t valid,
+                                             ScratchHeader *hdr, uint64_t n) {
     if (pos < bulk) return buf[pos];
-    if (pos < valid) return in[base + pos];
+    if (pos < valid && in_bounds(hdr, base + pos, 1, n)) return in[base + pos];
     return 0u;
 }
 
@@ -319,7 +320,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 } else if (AHEAD > 0) {
                     uint32_t valid, bulk;
                     tile_extent(t, valid, bulk);
-                    if (bulk) bulk_prefetch_l2(in + uint64_t(t) * TILE, bulk * 4u, keep);
+                    if (bulk && in_bounds(hdr, uint64_t(t) * TILE, bulk, n))
+                        bulk_prefetch_l2(in + uint64_t(t) * TILE, bulk * 4u, keep);
                 }
             }
             if (ok && k >= uint32_t(SIN))
@@ -329,7 +331,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 // tiles drawn but never loaded: poison them so no successor waits
                 for (uint32_t g = k; g < taken; ++g) {
                     const uint32_t t = ld_volatile_smem(sm.tile_id(int(g % RING)));
-                    if (t != kNoTile) st_relaxed_gpu(desc + t, make_desc(kPoison, 0u));
+                    if (t != kNoTile && in_bounds(hdr, t, 1, num_tiles))
+                        st_relaxed_gpu(desc + t, make_desc(kPoison, 0u));
                 }
                 stop_at(k - 1);
                 return;
@@ -342,7 +345,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             }
             uint32_t valid, bulk;
             tile_extent(t, valid, bulk);
-            if (bulk) {
+            if (bulk && in_bounds(hdr, uint64_t(t) * TILE, bulk, n) && in_bounds(hdr, 0, bulk, TILE)) {
                 mbar_arrive_expect_tx(sm.in_full(s), bulk * 4u);
                 bulk_load_hint(sm.in_data(s), in + uint64_t(t) * TILE, bulk * 4u, sm.in_full(s), keep);
             } else {
@@ -372,7 +375,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 if (!warp_wait(sm.in_full(s), use & 1u) && lane == 0)
                     record_error(hdr, DWP_ERR_PIPELINE_TIMEOUT);
                 if (lane == 0) {
-                    st_relaxed_gpu(desc + t, make_desc(kPoison, 0u));
+                    if (in_bounds(hdr, t, 1, num_tiles)) st_relaxed_gpu(desc + t, make_desc(kPoison, 0u));
                     *sm.lbres(i) = 1u;
                     mbar_arrive(sm.in_empty(s));
                     mbar_arrive(sm.info_ready(i));
@@ -412,7 +415,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             for (uint32_t kk = k0; kk <= nseg; kk += 32) {
                 const uint64_t idx = uint64_t(kk) + lane;
                 uint32_t p = 0xffffffffu;
-                if (idx <= nseg) p = stride == 1u ? smp[idx] : __ldg(off + idx);
+                if (idx <= nseg && in_bounds(hdr, idx, 1, uint64_t(nseg) + 1))
+                    p = stride == 1u ? smp[idx] : __ldg(off + idx);
                 if (idx <= nseg && uint64_t(p) >= base && uint64_t(p) < tend) {
                     const uint32_t r = uint32_t(uint64_t(p) - base);
                     atomicOr(&heads[r >> 5], 1u << (r & 31u));
@@ -467,7 +471,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                     }
                 } else if (c * ITEMS < valid) {
                     for (int j = 0; j < ITEMS; ++j) {
-                        const uint32_t x = seg_elem(buf, in, base, c * ITEMS + j, bulk, valid);
+                        const uint32_t x = seg_elem(buf, in, base, c * ITEMS + j, bulk, valid, hdr, n);
                         acc = ((hb >> j) & 1u) ? x : acc + x;
                     }
                 }
@@ -530,7 +534,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             }
             if (PERTURB) perturb(fault, t, kSiteAggregate);
             if (lane == 0) {
-                if (t != fault.never_publish_tile)
+                if (t != fault.never_publish_tile && in_bounds(hdr, t, 1, num_tiles))
                     st_relaxed_gpu(desc + t, make_desc((t == 0 || ah) ? kPrefix : kAggregate, av));
                 *sm.agg(i) = av;
                 *sm.agg_head(i) = ah;
@@ -597,7 +601,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             }
             if (PERTURB && rc == 0) perturb(fault, t, kSitePrefix);
             if (lane == 0) {
-                if (rc == 0) {
+                if (!in_bounds(hdr, t, 1, num_tiles)) {
+                    // debug bounds build only: no descriptor to publish
+                } else if (rc == 0) {
                     if (t != 0 && !ah && t != fault.never_publish_tile)
                         st_relaxed_gpu(desc + t, make_desc(kPrefix, carry + *sm.agg(i)));
                 } else {
@@ -640,7 +646,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             }
             uint32_t valid, bulk;
             tile_extent(t, valid, bulk);
-            if (bulk) {
+            if (bulk && in_bounds(hdr, uint64_t(t) * TILE, bulk, n) && in_bounds(hdr, 0, bulk, TILE)) {
                 mbar_arrive_expect_tx(sm.out_full(o), bulk * 4u);
                 bulk_load_hint(sm.out_data(o), in + uint64_t(t) * TILE, bulk * 4u, sm.out_full(o),
                                l2_policy_evict_first());
@@ -716,7 +722,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         } else if (p0 < valid) {
             for (int j = 0; j < ITEMS; ++j) {
                 const uint32_t pos = p0 + j;
-                const uint32_t x = seg_elem(buf, in, base, pos, bulk, valid);
+                const uint32_t x = seg_elem(buf, in, base, pos, bulk, valid, hdr, n);
                 if ((hb >> j) & 1u) acc = 0u;
                 uint32_t y;
                 if (INCL) {
@@ -729,7 +735,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 const uint64_t g = base + pos;
                 if (pos < valid && covered && pos < bulk)
                     buf[pos] = y;
-                else if (pos < valid && g >= cover_lo && g < cover_hi)
+                else if (pos < valid && g >= cover_lo && g < cover_hi && in_bounds(hdr, g, 1, n))
                     out[g] = y;
             }
         }
@@ -738,7 +744,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         if (lane == 0) {
             const uint32_t w0 = cw * WE;
             const uint32_t w1 = covered ? min(w0 + uint32_t(WE), bulk) : w0;
-            if (w1 > w0) {
+            if (w1 > w0 && in_bounds(hdr, base + w0, w1 - w0, n)) {
                 bulk_store_hint(out + base + w0, buf + w0, (w1 - w0) * 4u, l2_policy_evict_first());
                 bulk_commit();
                 bulk_wait_read<1>();

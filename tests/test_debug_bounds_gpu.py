@@ -1,10 +1,13 @@
-"""The plain scan in the debug bounds build (-DDWP_DEBUG_BOUNDS=1): every
-global access of both scan kernels is checked against its buffer first, and
+"""The plain scan, the segmented scan and compaction in the debug bounds
+build (-DDWP_DEBUG_BOUNDS=1): every global access of their kernels is
+checked against its buffer first, and
 an access that would leave it is skipped and reported as DWP_ERR_BOUNDS
 instead of being made.  Run over the sizes where index arithmetic is most
 likely to slip (tile and tier edges, ragged tails, the switch between the
-two kernels, in place, a rescued tile, a bounded window), the checked build
-must report no bounds error and still match the oracle."""
+two plain-scan kernels, in place, a rescued tile, a bounded window; for the
+segmented scan the global offset search and rows outside the segments; for
+compaction none, some and all records kept), the checked build must report
+no bounds error and still match the oracle."""
 import ctypes
 import os
 
@@ -111,3 +114,79 @@ def test_no_bounds_error_with_a_rescued_tile_and_a_window(lib, ref, n):
 
 def test_the_default_library_is_not_the_checked_one(lib):
     assert os.path.abspath(dwp.LIB_PATH) != os.path.abspath(BOUNDS_LIB)
+
+
+# ------------------------------------------------ segmented scan, compaction
+
+SENTINEL = 0xDEADBEEF
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def seg_run(lib, values, offsets, inclusive):
+    n, nseg = values.size, offsets.size - 1
+    v = torch.from_numpy(values.view(np.int32)).cuda()
+    o = torch.from_numpy(np.ascontiguousarray(offsets, dtype=np.uint32).view(np.int32)).cuda()
+    out = torch.full((n,), SENTINEL - (1 << 32), dtype=torch.int32, device="cuda")
+    sb = ctypes.c_size_t(0)
+    mode = dwp.DWP_INCLUSIVE if inclusive else dwp.DWP_EXCLUSIVE
+    assert lib.dwp_segmented_scan_u32(None, None, nseg, None, n, mode, None, ctypes.byref(sb), None) == 0
+    scratch = torch.empty(max(sb.value, 16), dtype=torch.uint8, device="cuda")
+    st = lib.dwp_segmented_scan_u32(ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(o.data_ptr()), nseg,
+                                    ctypes.c_void_p(out.data_ptr()), n, mode,
+                                    ctypes.c_void_p(scratch.data_ptr()), ctypes.byref(sb), _stream())
+    assert st == dwp.DWP_SUCCESS
+    status = lib.dwp_read_status(ctypes.c_void_p(scratch.data_ptr()), _stream())
+    return out.cpu().numpy().view(np.uint32), status
+
+
+def seg_cases():
+    yield "skewed 1", np.array([0, 1], np.uint32), 1
+    for n in (7167, 7168 * 3 + 5, (1 << 20) + 3):
+        yield "skewed %d" % n, synth.segment_offsets(n, seed=40 + n % 7), n
+    n = 7168 * 40 + 11  # more offsets than the per-block sample: the global search
+    yield "every 100 rows", np.append(np.arange(0, n, 100, dtype=np.uint32), np.uint32(n)), n
+    n = 7168 * 9 + 3  # rows outside the segments at both ends, empty segments
+    yield "uncovered ends", np.array([5, 5, 5, 7168, 7169, 7169, 30000, n - 7], np.uint32), n
+
+
+@pytest.mark.parametrize("inclusive", [False, True])
+def test_segmented_scan_no_bounds_error(lib, ref, inclusive):
+    for name, offsets, n in seg_cases():
+        values = synth.u32_byte_values(n, seed=50 + n % 13)
+        got, status = seg_run(lib, values, offsets, inclusive)
+        assert status == dwp.DWP_SUCCESS, (name, dwp.status_string(status))
+        want = ref.segmented_scan_u32(values, offsets, inclusive, out=np.full(n, SENTINEL, np.uint32))
+        assert np.array_equal(got, want), name
+
+
+def compact_run(lib, rec, flags):
+    n = flags.size
+    r = torch.from_numpy(rec.view(np.int32)).cuda()
+    f = torch.from_numpy(flags).cuda()
+    out = torch.full_like(r, SENTINEL - (1 << 32))
+    cnt = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sb = ctypes.c_size_t(0)
+    assert lib.dwp_compact_by_flags(None, None, n, None, None, None, ctypes.byref(sb), None) == 0
+    scratch = torch.empty(max(sb.value, 16), dtype=torch.uint8, device="cuda")
+    st = lib.dwp_compact_by_flags(ctypes.c_void_p(r.data_ptr()), ctypes.c_void_p(f.data_ptr()), n,
+                                  ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(cnt.data_ptr()),
+                                  ctypes.c_void_p(scratch.data_ptr()), ctypes.byref(sb), _stream())
+    assert st == dwp.DWP_SUCCESS
+    status = lib.dwp_read_status(ctypes.c_void_p(scratch.data_ptr()), _stream())
+    return out.cpu().numpy().view(np.uint32), int(cnt.item()), status
+
+
+@pytest.mark.parametrize("n", [1, 17, 2559, 2560, 2561, 2560 * 37 + 5, (1 << 20) + 3])
+@pytest.mark.parametrize("p", [0.0, 0.3, 1.0])
+def test_compaction_no_bounds_error(lib, ref, n, p):
+    rec = synth.records(n, seed=60 + n % 11)
+    flags = synth.keep_flags(n, p=p, seed=61 + n % 5)
+    got, k, status = compact_run(lib, rec, flags)
+    assert status == dwp.DWP_SUCCESS, dwp.status_string(status)
+    want, kw = ref.compact(rec, flags)
+    assert k == kw
+    assert np.array_equal(got[:k], want[:k])
+    assert (got[k:] == SENTINEL).all()
