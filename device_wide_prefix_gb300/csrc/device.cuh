@@ -229,9 +229,9 @@ __device__ __forceinline__ void record_error(ScratchHeader *hdr, uint32_t code) 
 }
 
 // Debug bounds build (compile with -DDWP_DEBUG_BOUNDS=1).  Before each
-// global access, the plain-scan, segmented-scan and compaction kernels ask
-// whether elements [first, first + count) lie inside a buffer of `extent`
-// elements.  An access that would leave its buffer is skipped and
+// global access, the look-back kernels (plain and segmented scan,
+// compaction, recurrence, segmented reduction) ask whether elements
+// [first, first + count) lie inside a buffer of `extent` elements.  An access that would leave its buffer is skipped and
 // DWP_ERR_BOUNDS is recorded in the status word: a checked run reports a bad
 // index instead of faulting.  The default build compiles every check to
 // `true`.

@@ -163,11 +163,12 @@ struct RecSmem {
 // identity map (a = 1, b = 0).
 __device__ __forceinline__ void rec_elem(const float *sa, const float *sb, const float *ga,
                                          const float *gb, uint64_t base, uint32_t pos,
-                                         uint32_t bulk, uint32_t valid, float &av, float &bv) {
+                                         uint32_t bulk, uint32_t valid, float &av, float &bv,
+                                         ScratchHeader *hdr, uint64_t n) {
     if (pos < bulk) {
         av = sa[pos];
         bv = sb[pos];
-    } else if (pos < valid) {
+    } else if (pos < valid && in_bounds(hdr, base + pos, 1, n)) {
         av = ga[base + pos];
         bv = gb[base + pos];
     } else {
@@ -415,7 +416,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 } else if (AHEAD > 0) {
                     uint32_t valid, bulk;
                     tile_extent(t, valid, bulk);
-                    if (bulk) {
+                    if (bulk && in_bounds(hdr, uint64_t(t) * TILE, bulk, n)) {
                         bulk_prefetch_l2(ga + uint64_t(t) * TILE, bulk * 4u, keep);
                         bulk_prefetch_l2(gb + uint64_t(t) * TILE, bulk * 4u, keep);
                     }
@@ -427,7 +428,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 record_error(hdr, DWP_ERR_PIPELINE_TIMEOUT);
                 for (uint32_t g = k; g < taken; ++g) {
                     const uint32_t t = ld_volatile_smem(sm.tile_id(int(g % RING)));
-                    if (t != kNoTile) st_relaxed_gpu(desc + 2 * uint64_t(t) + 1, make_desc(kPoison, 0u));
+                    if (t != kNoTile && in_bounds(hdr, t, 1, num_tiles))
+                        st_relaxed_gpu(desc + 2 * uint64_t(t) + 1, make_desc(kPoison, 0u));
                 }
                 stop_at(k - 1);
                 return;
@@ -439,7 +441,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             }
             uint32_t valid, bulk;
             tile_extent(t, valid, bulk);
-            if (bulk) {
+            if (bulk && in_bounds(hdr, uint64_t(t) * TILE, bulk, n) && in_bounds(hdr, 0, bulk, TILE)) {
                 mbar_arrive_expect_tx(sm.in_full(s), 2u * bulk * 4u);
                 bulk_load_hint(sm.in_a(s), ga + uint64_t(t) * TILE, bulk * 4u, sm.in_full(s), keep);
                 bulk_load_hint(sm.in_b(s), gb + uint64_t(t) * TILE, bulk * 4u, sm.in_full(s), keep);
@@ -468,7 +470,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             }
             if (ld_volatile_smem(sm.abort_flag()) != 0) {
                 if (lane == 0) {
-                    st_relaxed_gpu(desc + 2 * uint64_t(t) + 1, make_desc(kPoison, 0u));
+                    if (in_bounds(hdr, t, 1, num_tiles))
+                        st_relaxed_gpu(desc + 2 * uint64_t(t) + 1, make_desc(kPoison, 0u));
                     *sm.lbres(i) = 1u;
                     mbar_arrive(sm.in_empty(s));
                     mbar_arrive(sm.info_ready(i));
@@ -507,7 +510,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 } else if (c * ITEMS < valid) {
                     for (int j = 0; j < ITEMS; ++j) {
                         float av, bv;
-                        rec_elem(sa, sb, ga, gb, base, c * ITEMS + j, bulk, valid, av, bv);
+                        rec_elem(sa, sb, ga, gb, base, c * ITEMS + j, bulk, valid, av, bv, hdr, n);
                         B = __fmaf_rn(av, B, bv);
                         A = __fmul_rn(av, A);
                     }
@@ -558,7 +561,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             }
             if (PERTURB) perturb(fault, t, kSiteAggregate);
             if (lane == 0) {
-                if (t != fault.never_publish_tile) {
+                if (t != fault.never_publish_tile && in_bounds(hdr, t, 1, num_tiles)) {
                     if (t == 0) {
                         st_relaxed_gpu(desc + 1, make_desc(kPrefix, __float_as_uint(gB)));
                     } else {
@@ -613,7 +616,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             if (ld_volatile_smem(sm.lbres(i)) != 0u) rc = 1;
             if (PERTURB && rc == 0) perturb(fault, t, kSitePrefix);
             if (lane == 0) {
-                if (rc == 0) {
+                if (!in_bounds(hdr, t, 1, num_tiles)) {
+                    // debug bounds build only: no descriptor to publish
+                } else if (rc == 0) {
                     if (t != 0 && t != fault.never_publish_tile)
                         st_relaxed_gpu(desc + 2 * uint64_t(t) + 1,
                                        make_desc(kPrefix, __float_as_uint(
@@ -659,7 +664,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             }
             uint32_t valid, bulk;
             tile_extent(t, valid, bulk);
-            if (bulk) {
+            if (bulk && in_bounds(hdr, uint64_t(t) * TILE, bulk, n) && in_bounds(hdr, 0, bulk, TILE)) {
                 mbar_arrive_expect_tx(sm.out_full(o), 2u * bulk * 4u);
                 bulk_load_hint(sm.out_a(o), ga + uint64_t(t) * TILE, bulk * 4u, sm.out_full(o), drop);
                 bulk_load_hint(sm.out_b(o), gb + uint64_t(t) * TILE, bulk * 4u, sm.out_full(o), drop);
@@ -729,7 +734,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             for (int jj = 0; jj < ITEMS; ++jj) {
                 const uint32_t pos = p0 + jj;
                 float av, bv;
-                rec_elem(sa, sb, ga, gb, base, pos, bulk, valid, av, bv);
+                rec_elem(sa, sb, ga, gb, base, pos, bulk, valid, av, bv, hdr, n);
                 float y;
                 if (INCL) {
                     h = __fmaf_rn(av, h, bv);
@@ -740,7 +745,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 }
                 if (pos < bulk)
                     sb[pos] = y;
-                else if (pos < valid)
+                else if (pos < valid && in_bounds(hdr, base + pos, 1, n))
                     out[base + pos] = y;
             }
         }
@@ -749,7 +754,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         if (lane == 0) {
             const uint32_t w0 = cw * WE;
             const uint32_t w1 = min(w0 + uint32_t(WE), bulk);
-            if (w1 > w0) {
+            if (w1 > w0 && in_bounds(hdr, base + w0, w1 - w0, n)) {
                 bulk_store_hint(out + base + w0, sb + w0, (w1 - w0) * 4u, l2_policy_evict_first());
                 bulk_commit();
                 bulk_wait_read<1>();

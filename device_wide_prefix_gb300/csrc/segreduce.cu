@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         const uint64_t rem = n - uint64_t(t) * TILE;
         const uint32_t valid = rem < uint64_t(TILE) ? uint32_t(rem) : uint32_t(TILE);
         const uint32_t bulk = valid == uint32_t(TILE) ? valid : (valid & ~3u);
-        if (bulk) {
+        if (bulk && in_bounds(hdr, uint64_t(t) * TILE, bulk, n) && in_bounds(hdr, 0, bulk, TILE)) {
             mbar_arrive_expect_tx(sm.full(j), bulk * 4u);
             bulk_load_hint(sm.stage(j), in + uint64_t(t) * TILE, bulk * 4u, sm.full(j),
                            l2_policy_evict_first());
@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         const uint32_t *buf = sm.stage(j);
         auto row = [&](uint32_t q) -> uint32_t {  // row b + q of the tile
             if (q < bulk) return buf[q];
-            if (q < valid) return in[b + q];
+            if (q < valid && in_bounds(hdr, b + q, 1, n)) return in[b + q];
             return 0u;
         };
         uint32_t *pre = sm.pre();
@@ -197,11 +197,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         };
         for (uint32_t s0 = s_lo; s0 < s_hi; s0 += 32u) {
             const uint32_t s = s0 + lane;
-            if (s < s_hi) {
+            if (s < s_hi && in_bounds(hdr, s, 2, uint64_t(nseg) + 1)) {
                 const uint64_t o0 = __ldg(off + s), o1 = __ldg(off + s + 1);
                 const uint64_t lo = o0 > b ? o0 : b;
                 const uint64_t hi = o1 < e ? o1 : e;
-                if (hi > lo) {
+                if (hi > lo && in_bounds(hdr, s, 1, nseg)) {
                     uint32_t sum = prefix(uint32_t(hi - 1 - b));
                     if (lo > b) sum -= prefix(uint32_t(lo - 1 - b));
                     if (o0 >= b && o1 <= e)

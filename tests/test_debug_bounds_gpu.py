@@ -1,13 +1,14 @@
-"""The plain scan, the segmented scan and compaction in the debug bounds
-build (-DDWP_DEBUG_BOUNDS=1): every global access of their kernels is
-checked against its buffer first, and
-an access that would leave it is skipped and reported as DWP_ERR_BOUNDS
-instead of being made.  Run over the sizes where index arithmetic is most
-likely to slip (tile and tier edges, ragged tails, the switch between the
-two plain-scan kernels, in place, a rescued tile, a bounded window; for the
-segmented scan the global offset search and rows outside the segments; for
-compaction none, some and all records kept), the checked build must report
-no bounds error and still match the oracle."""
+"""The look-back kernels in the debug bounds build (-DDWP_DEBUG_BOUNDS=1):
+the plain scan, the segmented scan, compaction, the linear recurrence and
+the segmented reduction check every global access against its buffer
+first, and an access that would leave it is skipped and reported as
+DWP_ERR_BOUNDS instead of being made.  The checked build runs over the
+sizes where index arithmetic is most likely to slip: tile and tier edges,
+ragged tails, the switch between the two plain-scan kernels, in place, a
+rescued tile and a bounded window; for the segmented scan and reduction the
+global offset search and rows outside the segments; for compaction none,
+some and all records kept.  It must report no bounds error and still match
+the oracle."""
 import ctypes
 import os
 
@@ -190,3 +191,57 @@ def test_compaction_no_bounds_error(lib, ref, n, p):
     assert k == kw
     assert np.array_equal(got[:k], want[:k])
     assert (got[k:] == SENTINEL).all()
+
+
+# ------------------------------------ linear recurrence, segmented reduction
+
+
+def rec_run(lib, a, b, inclusive):
+    n = a.size
+    ta, tb = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
+    h = torch.full_like(tb, 12345.0)
+    sb = ctypes.c_size_t(0)
+    mode = dwp.DWP_INCLUSIVE if inclusive else dwp.DWP_EXCLUSIVE
+    assert lib.dwp_linear_recurrence_f32(None, None, None, n, mode, None, ctypes.byref(sb), None) == 0
+    scratch = torch.empty(max(sb.value, 16), dtype=torch.uint8, device="cuda")
+    st = lib.dwp_linear_recurrence_f32(ctypes.c_void_p(ta.data_ptr()), ctypes.c_void_p(tb.data_ptr()),
+                                       ctypes.c_void_p(h.data_ptr()), n, mode,
+                                       ctypes.c_void_p(scratch.data_ptr()), ctypes.byref(sb), _stream())
+    assert st == dwp.DWP_SUCCESS
+    status = lib.dwp_read_status(ctypes.c_void_p(scratch.data_ptr()), _stream())
+    return h.cpu().numpy(), status
+
+
+@pytest.mark.parametrize("inclusive", [False, True])
+def test_recurrence_no_bounds_error(lib, ref, inclusive):
+    for n in (1, 5, 4607, 4608, 4609, 4608 * 200 + 3, (1 << 22) + 1):
+        a = synth.decay_values(n, seed=70 + n % 7)
+        b = synth.f32_values(n, seed=71 + n % 5)
+        got, status = rec_run(lib, a, b, inclusive)
+        assert status == dwp.DWP_SUCCESS, (n, dwp.status_string(status))
+        want, g = ref.linear_recurrence(a, b, inclusive)
+        assert (np.abs(got.astype(np.float64) - want) <= 1e-4 * g + 1e-6).all(), n
+
+
+def red_run(lib, values, offsets):
+    n, nseg = values.size, offsets.size - 1
+    v = torch.from_numpy(values.view(np.int32)).cuda()
+    o = torch.from_numpy(np.ascontiguousarray(offsets, dtype=np.uint32).view(np.int32)).cuda()
+    out = torch.full((max(nseg, 1),), SENTINEL - (1 << 32), dtype=torch.int32, device="cuda")
+    sb = ctypes.c_size_t(0)
+    assert lib.dwp_segmented_reduce_u32(None, None, nseg, None, n, None, ctypes.byref(sb), None) == 0
+    scratch = torch.empty(max(sb.value, 16), dtype=torch.uint8, device="cuda")
+    st = lib.dwp_segmented_reduce_u32(ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(o.data_ptr()), nseg,
+                                      ctypes.c_void_p(out.data_ptr()), n,
+                                      ctypes.c_void_p(scratch.data_ptr()), ctypes.byref(sb), _stream())
+    assert st == dwp.DWP_SUCCESS
+    status = lib.dwp_read_status(ctypes.c_void_p(scratch.data_ptr()), _stream())
+    return out.cpu().numpy().view(np.uint32)[:nseg], status
+
+
+def test_segmented_reduction_no_bounds_error(lib, ref):
+    for name, offsets, n in seg_cases():
+        values = synth.u32_byte_values(n, seed=80 + n % 13)
+        got, status = red_run(lib, values, offsets)
+        assert status == dwp.DWP_SUCCESS, (name, dwp.status_string(status))
+        assert np.array_equal(got, ref.segmented_reduce_u32(values, offsets)), name
