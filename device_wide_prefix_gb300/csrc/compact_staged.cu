@@ -52,10 +52,12 @@ __global__ void __launch_bounds__(kStagedThreads)
 
 // out[off[i]] = rec[i] for kept records; 4 records per thread and step (one
 // 16-byte load each of f and off), the last n % 4 one by one.  The thread
-// that handles record n - 1 writes the count.
+// that handles record n - 1 writes the count.  The output slot comes from
+// the scan, so the debug bounds build checks it (against n, in the scan's
+// status word).
 __global__ void __launch_bounds__(kStagedThreads)
     scatter_kernel(const uint4 *rec, const uint32_t *f, const uint32_t *off, uint64_t n, uint4 *out,
-                   uint32_t *count) {
+                   uint32_t *count, ScratchHeader *hdr) {
     pdl_wait();
     pdl_trigger();
     const uint64_t nvec = n / 4;
@@ -67,12 +69,12 @@ __global__ void __launch_bounds__(kStagedThreads)
         const uint32_t ok[4] = {ov.x, ov.y, ov.z, ov.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-            if (fk[j]) out[ok[j]] = rec[4 * q + j];
+            if (fk[j] && in_bounds(hdr, ok[j], 1, n)) out[ok[j]] = rec[4 * q + j];
         if (4 * q + 4 == n) *count = ok[3] + fk[3];
     }
     const uint64_t i = 4 * nvec + uint64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i < n && i < 4 * nvec + 4) {
-        if (f[i]) out[off[i]] = rec[i];
+        if (f[i] && in_bounds(hdr, off[i], 1, n)) out[off[i]] = rec[i];
         if (i == n - 1) *count = off[i] + f[i];
     }
 }
@@ -159,7 +161,7 @@ extern "C" dwp_status dwp_compact_by_flags_staged(const void *d_records, const u
     if (launch_pdl(scatter_kernel, dim3(g3), dim3(kStagedThreads), 0, s,
                    static_cast<const uint4 *>(d_records), static_cast<const uint32_t *>(f),
                    static_cast<const uint32_t *>(off), uint64_t(n), static_cast<uint4 *>(d_out),
-                   d_count) != cudaSuccess) {
+                   d_count, static_cast<ScratchHeader *>(d_scratch)) != cudaSuccess) {
         cudaGetLastError();
         return DWP_ERR_CUDA;
     }

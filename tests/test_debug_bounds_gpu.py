@@ -245,3 +245,27 @@ def test_segmented_reduction_no_bounds_error(lib, ref):
         got, status = red_run(lib, values, offsets)
         assert status == dwp.DWP_SUCCESS, (name, dwp.status_string(status))
         assert np.array_equal(got, ref.segmented_reduce_u32(values, offsets)), name
+
+
+@pytest.mark.parametrize("n", [1, 2561, 2560 * 37 + 5, (1 << 20) + 3])
+def test_staged_compaction_no_bounds_error(lib, ref, n):
+    """The staged form's scatter writes to slots its own scan computed."""
+    rec = synth.records(n, seed=90 + n % 11)
+    flags = synth.keep_flags(n, seed=91 + n % 5)
+    r = torch.from_numpy(rec.view(np.int32)).cuda()
+    f = torch.from_numpy(flags).cuda()
+    out = torch.full_like(r, SENTINEL - (1 << 32))
+    cnt = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sb = ctypes.c_size_t(0)
+    assert lib.dwp_compact_by_flags_staged(None, None, n, None, None, None, ctypes.byref(sb), None) == 0
+    scratch = torch.empty(max(sb.value, 16), dtype=torch.uint8, device="cuda")
+    st = lib.dwp_compact_by_flags_staged(ctypes.c_void_p(r.data_ptr()), ctypes.c_void_p(f.data_ptr()), n,
+                                         ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(cnt.data_ptr()),
+                                         ctypes.c_void_p(scratch.data_ptr()), ctypes.byref(sb), _stream())
+    assert st == dwp.DWP_SUCCESS
+    assert lib.dwp_read_status(ctypes.c_void_p(scratch.data_ptr()), _stream()) == dwp.DWP_SUCCESS
+    want, k = ref.compact(rec, flags)
+    got = out.cpu().numpy().view(np.uint32)
+    assert int(cnt.item()) == k
+    assert np.array_equal(got[:k], want[:k])
+    assert (got[k:] == SENTINEL).all()
