@@ -782,13 +782,16 @@ def measure_compact(dwp, lib, dev, stream, peaks, log2n=26, steps=100, warmup=5)
                         "(SplitMix64 seed 0xD3B00004)" % log2n}
 
 
-def kept_sector_bytes(flags: np.ndarray) -> int:
-    """Bytes of the 32-byte sectors that hold at least one kept 16-byte
-    record: what a compaction that reads only the kept records must read."""
+def kept_sector_bytes(flags: np.ndarray, unit: int = 32) -> int:
+    """Bytes of the `unit`-byte pieces of the record array that hold at least
+    one kept 16-byte record: what a compaction that reads only the kept
+    records must read when memory moves `unit` bytes at a time (32 for an L2
+    sector; about 128 for what DRAM moved in a probe of this workload)."""
+    per = unit // 16
     f = flags != 0
-    if f.size % 2:
-        f = np.concatenate([f, [False]])
-    return int(f.reshape(-1, 2).any(axis=1).sum()) * 32
+    if f.size % per:
+        f = np.concatenate([f, np.zeros(per - f.size % per, dtype=bool)])
+    return int(f.reshape(-1, per).any(axis=1).sum()) * unit
 
 
 def measure_compact_staged(dwp, lib, dev, stream, peaks, log2n=26, steps=50, warmup=5) -> dict:
@@ -836,6 +839,13 @@ def measure_compact_staged(dwp, lib, dev, stream, peaks, log2n=26, steps=50, war
     res["selective_read_lower_bound"] = {
         "bytes": lower, "ms_at_peak": lower / (peaks["hbm_gbs"] * 1e9) * 1e3,
         "fused_frac_of_it": lower / (res["fused"]["ms"] * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+    # the same bound in 128-byte pieces: at p = 0.3 reading only the kept
+    # records measured no faster than reading them all
+    line = kept_sector_bytes(flags_np, 128)
+    lower128 = n + line + 16 * k + 4
+    res["selective_read_lower_bound_128B"] = {
+        "bytes": lower128, "ms_at_peak": lower128 / (peaks["hbm_gbs"] * 1e9) * 1e3,
+        "fused_frac_of_it": lower128 / (res["fused"]["ms"] * 1e-3) / 1e9 / peaks["hbm_gbs"]}
     res["staged_over_fused"] = res["staged"]["ms"] / res["fused"]["ms"]
     res["extra_bytes_staged"] = res["staged"]["algorithmic_bytes"] - res["fused"]["algorithmic_bytes"]
     return res
