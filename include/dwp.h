@@ -288,7 +288,8 @@ dwp_status dwp_linear_recurrence_f32(const float *d_a, const float *d_b, float *
 /*
  * Device-side status of the most recent call that used d_scratch.
  * Synchronises `stream`, then reads the status word.  Returns DWP_SUCCESS,
- * DWP_ERR_LOOKBACK_TIMEOUT or DWP_ERR_PIPELINE_TIMEOUT; DWP_ERR_CUDA if the
+ * DWP_ERR_LOOKBACK_TIMEOUT or DWP_ERR_PIPELINE_TIMEOUT (and, in a library
+ * built with -DDWP_DEBUG_BOUNDS=1, DWP_ERR_BOUNDS); DWP_ERR_CUDA if the
  * synchronisation or the read fails; DWP_ERR_INVALID_VALUE for NULL.
  */
 dwp_status dwp_read_status(const void *d_scratch, dwp_stream stream);
